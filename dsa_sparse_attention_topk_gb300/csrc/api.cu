@@ -1,0 +1,199 @@
+// C ABI entry points (include/dsa.h): argument checking, the device status word and
+// the per-thread error message.  Every compute step runs in the kernels behind
+// dsa_launch.h; nothing here touches tensor data on the host.
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "dsa_common.cuh"
+#include "dsa_launch.h"
+
+namespace {
+
+__device__ unsigned g_status_word;
+
+thread_local std::string t_last_error;
+
+int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device address of the status word, looked up once per device with that device current.
+unsigned* status_ptr() {
+  static std::mutex mu;
+  static unsigned* ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int dsa_version(void) { return 100; }
+
+const char* dsa_last_error(void) { return t_last_error.c_str(); }
+
+int dsa_quant_kv_mxfp8(const void* k_bf16, const int64_t* slot_mapping, int32_t n_tokens,
+                       uint8_t* k_cache, int64_t num_slots, void* stream) {
+  if (n_tokens < 0) return fail(DSA_ERR_INVALID_ARG, "quant_kv_mxfp8: n_tokens < 0");
+  if (n_tokens == 0) return DSA_OK;
+  if (!k_bf16 || !slot_mapping || !k_cache) return fail(DSA_ERR_INVALID_ARG, "quant_kv_mxfp8: null pointer");
+  if (!aligned(k_bf16, 16) || !aligned(k_cache, 16) || !aligned(slot_mapping, 8))
+    return fail(DSA_ERR_INVALID_ARG, "quant_kv_mxfp8: k_bf16/k_cache must be 16-byte aligned");
+  if (num_slots <= 0 || num_slots % DSA_PAGE_SIZE)
+    return fail(DSA_ERR_INVALID_ARG, "quant_kv_mxfp8: num_slots must be a positive multiple of 64");
+  unsigned* st = status_ptr();
+  if (!st) return fail(DSA_ERR_CUDA, "quant_kv_mxfp8: no CUDA device");
+  cudaError_t e = dsa::launch_quant_mxfp8(k_bf16, slot_mapping, n_tokens, k_cache, num_slots, st,
+                                          static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSA_OK : cuda_fail(e, "quant_kv_mxfp8 launch");
+}
+
+int dsa_quant_kv_fp8(const void* kv_bf16, const int64_t* slot_mapping, int32_t n_tokens,
+                     uint8_t* kv_cache, int64_t num_slots, void* stream) {
+  if (n_tokens < 0) return fail(DSA_ERR_INVALID_ARG, "quant_kv_fp8: n_tokens < 0");
+  if (n_tokens == 0) return DSA_OK;
+  if (!kv_bf16 || !slot_mapping || !kv_cache) return fail(DSA_ERR_INVALID_ARG, "quant_kv_fp8: null pointer");
+  if (!aligned(kv_bf16, 16) || !aligned(kv_cache, 16) || !aligned(slot_mapping, 8))
+    return fail(DSA_ERR_INVALID_ARG, "quant_kv_fp8: kv_bf16/kv_cache must be 16-byte aligned");
+  if (num_slots <= 0 || num_slots % DSA_PAGE_SIZE)
+    return fail(DSA_ERR_INVALID_ARG, "quant_kv_fp8: num_slots must be a positive multiple of 64");
+  unsigned* st = status_ptr();
+  if (!st) return fail(DSA_ERR_CUDA, "quant_kv_fp8: no CUDA device");
+  cudaError_t e = dsa::launch_quant_fp8(kv_bf16, slot_mapping, n_tokens, kv_cache, num_slots, st,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSA_OK : cuda_fail(e, "quant_kv_fp8 launch");
+}
+
+static int check_indexer(const char* who, const void* q_bf16, const float* w, int32_t n_q, int32_t h_i,
+                         int32_t q_group, const uint8_t* k_cache, int64_t num_pages,
+                         const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                         const int32_t* q_seq, const int32_t* q_pos, int32_t n_seq, int32_t max_ctx) {
+  if (n_q < 0 || n_seq < 0) return fail(DSA_ERR_INVALID_ARG, "%s: negative n_q or n_seq", who);
+  if (h_i < 1 || h_i > 64) return fail(DSA_ERR_UNSUPPORTED, "%s: h_i must be 1..64 (got %d)", who, h_i);
+  if (q_group < 1 || q_group > 4) return fail(DSA_ERR_UNSUPPORTED, "%s: q_group must be 1..4", who);
+  if (q_group * h_i > 256) return fail(DSA_ERR_UNSUPPORTED, "%s: q_group * h_i must be <= 256", who);
+  if (n_q % q_group) return fail(DSA_ERR_INVALID_ARG, "%s: n_q must be a multiple of q_group", who);
+  if (max_ctx < 1 || max_ctx > 262144) return fail(DSA_ERR_UNSUPPORTED, "%s: max_ctx must be 1..262144", who);
+  if (max_pages < (max_ctx + DSA_PAGE_SIZE - 1) / DSA_PAGE_SIZE)
+    return fail(DSA_ERR_INVALID_ARG, "%s: max_pages < ceil(max_ctx / 64)", who);
+  if (num_pages < 1) return fail(DSA_ERR_INVALID_ARG, "%s: num_pages must be >= 1", who);
+  if (n_q == 0) return DSA_OK;
+  if (!q_bf16 || !w || !k_cache || !page_table || !seq_lens || !q_seq || !q_pos)
+    return fail(DSA_ERR_INVALID_ARG, "%s: null pointer", who);
+  if (!aligned(q_bf16, 16) || !aligned(k_cache, 16) || !aligned(w, 4))
+    return fail(DSA_ERR_INVALID_ARG, "%s: q_bf16 and k_cache must be 16-byte aligned", who);
+  return DSA_OK;
+}
+
+int dsa_indexer_topk(const void* q_bf16, const float* w, int32_t n_q, int32_t h_i,
+                     int32_t q_group, const uint8_t* k_cache, int64_t num_pages,
+                     const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                     const int32_t* q_seq, const int32_t* q_pos, int32_t n_seq,
+                     int32_t max_ctx, int32_t topk, int32_t* out_idx, float* out_scores,
+                     void* stream) {
+  int rc = check_indexer("indexer_topk", q_bf16, w, n_q, h_i, q_group, k_cache, num_pages, page_table,
+                         max_pages, seq_lens, q_seq, q_pos, n_seq, max_ctx);
+  if (rc) return rc;
+  if (topk < 1 || topk > 2048) return fail(DSA_ERR_UNSUPPORTED, "indexer_topk: topk must be 1..2048");
+  if (n_q == 0) return DSA_OK;
+  if (!out_idx) return fail(DSA_ERR_INVALID_ARG, "indexer_topk: out_idx is null");
+  unsigned* st = status_ptr();
+  if (!st) return fail(DSA_ERR_CUDA, "indexer_topk: no CUDA device");
+  dsa::IndexerArgs a{q_bf16, w, n_q, h_i, q_group, k_cache, num_pages, page_table, max_pages,
+                     seq_lens, q_seq, q_pos, n_seq, max_ctx, topk, out_idx, out_scores, nullptr, st};
+  const char* why = nullptr;
+  cudaError_t e = dsa::launch_indexer(a, static_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess) return why ? fail(DSA_ERR_UNSUPPORTED, "%s", why) : cuda_fail(e, "indexer_topk launch");
+  return DSA_OK;
+}
+
+int dsa_indexer_scores(const void* q_bf16, const float* w, int32_t n_q, int32_t h_i,
+                       int32_t q_group, const uint8_t* k_cache, int64_t num_pages,
+                       const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                       const int32_t* q_seq, const int32_t* q_pos, int32_t n_seq,
+                       int32_t max_ctx, float* out_scores, void* stream) {
+  int rc = check_indexer("indexer_scores", q_bf16, w, n_q, h_i, q_group, k_cache, num_pages, page_table,
+                         max_pages, seq_lens, q_seq, q_pos, n_seq, max_ctx);
+  if (rc) return rc;
+  if (n_q == 0) return DSA_OK;
+  if (!out_scores) return fail(DSA_ERR_INVALID_ARG, "indexer_scores: out_scores is null");
+  unsigned* st = status_ptr();
+  if (!st) return fail(DSA_ERR_CUDA, "indexer_scores: no CUDA device");
+  dsa::IndexerArgs a{q_bf16, w, n_q, h_i, q_group, k_cache, num_pages, page_table, max_pages,
+                     seq_lens, q_seq, q_pos, n_seq, max_ctx, 1, nullptr, nullptr, out_scores, st};
+  const char* why = nullptr;
+  cudaError_t e = dsa::launch_indexer(a, static_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess) return why ? fail(DSA_ERR_UNSUPPORTED, "%s", why) : cuda_fail(e, "indexer_scores launch");
+  return DSA_OK;
+}
+
+size_t dsa_sparse_attn_workspace_size(int32_t n_q, int32_t h_s, int32_t topk) {
+  if (n_q <= 0 || h_s <= 0 || topk <= 0) return 0;
+  return dsa::sfa_workspace_bytes(n_q, h_s, topk);
+}
+
+int dsa_sparse_attn(const void* q_bf16, int32_t n_q, int32_t h_s, const uint8_t* kv_cache,
+                    int64_t num_pages, const int32_t* page_table, int32_t max_pages,
+                    const int32_t* seq_lens, const int32_t* q_seq, int32_t n_seq,
+                    const int32_t* topk_idx, int32_t topk, float sm_scale, void* out_bf16,
+                    float* out_lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (n_q < 0 || n_seq < 0) return fail(DSA_ERR_INVALID_ARG, "sparse_attn: negative n_q or n_seq");
+  if (h_s < 1 || h_s > 128) return fail(DSA_ERR_UNSUPPORTED, "sparse_attn: h_s must be 1..128");
+  if (topk < 1 || topk > 65536) return fail(DSA_ERR_UNSUPPORTED, "sparse_attn: topk must be 1..65536");
+  if (max_pages < 1 || num_pages < 1) return fail(DSA_ERR_INVALID_ARG, "sparse_attn: max_pages and num_pages must be >= 1");
+  if (!(sm_scale > 0.f) || sm_scale != sm_scale) return fail(DSA_ERR_INVALID_ARG, "sparse_attn: sm_scale must be positive");
+  if (n_q == 0) return DSA_OK;
+  if (!q_bf16 || !kv_cache || !page_table || !seq_lens || !q_seq || !topk_idx || !out_bf16)
+    return fail(DSA_ERR_INVALID_ARG, "sparse_attn: null pointer");
+  if (!aligned(q_bf16, 16) || !aligned(kv_cache, 16) || !aligned(out_bf16, 16))
+    return fail(DSA_ERR_INVALID_ARG, "sparse_attn: q, kv_cache and out must be 16-byte aligned");
+  const size_t need = dsa::sfa_workspace_bytes(n_q, h_s, topk);
+  if (need && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
+    return fail(DSA_ERR_INVALID_ARG, "sparse_attn: workspace must be >= %zu bytes and 256-byte aligned", need);
+  unsigned* st = status_ptr();
+  if (!st) return fail(DSA_ERR_CUDA, "sparse_attn: no CUDA device");
+  dsa::SfaArgs a{q_bf16, n_q, h_s, kv_cache, num_pages, page_table, max_pages, seq_lens, q_seq, n_seq,
+                 topk_idx, topk, sm_scale, out_bf16, out_lse, workspace, workspace_bytes, st};
+  const char* why = nullptr;
+  cudaError_t e = dsa::launch_sfa(a, static_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess) return why ? fail(DSA_ERR_UNSUPPORTED, "%s", why) : cuda_fail(e, "sparse_attn launch");
+  return DSA_OK;
+}
+
+int dsa_device_status(void* stream) {
+  unsigned* st = status_ptr();
+  if (!st) return fail(DSA_ERR_CUDA, "device_status: no CUDA device");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, st, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(st, 0, sizeof(unsigned), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "device_status");
+  return static_cast<int>(v);
+}
+
+}  // extern "C"

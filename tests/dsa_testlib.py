@@ -1,0 +1,190 @@
+"""Shared helpers of the tests: device upload of a workload through the library's own
+cache writers, oracle evaluation of sampled rows, and the parity criteria.
+
+Parity criteria (the method's stated tolerances):
+* indexer scores: |s_gpu - s_ref| <= 1e-3 * max(|s_ref|, D), where D = sum_h |w_h| *
+  |q_hat_h . k_hat| is the no-cancellation size of the score (so near-zero sums are not
+  judged against a zero denominator);
+* Top-K: the GPU index set equals the oracle's, except at positions whose oracle score
+  lies within 1e-3 (relative, same denominator) of the oracle's K-th score; the set size
+  is exactly min(K, n) with no duplicates and -1 everywhere else;
+* SFA: bf16 output within max-abs 2e-2 and mean-abs 2e-3 of the float64 oracle.
+"""
+
+import numpy as np
+import torch
+
+import oracle
+from oracle.indexer import indexer_magnitude_row, selectable_count
+
+SCORE_RTOL = 1e-3
+SFA_MAX_ABS = 2e-2
+SFA_MEAN_ABS = 2e-3
+
+
+def ensure_built():
+    import dsa_sparse_attention_topk_gb300 as dsa
+    import os
+    if not os.path.exists(dsa.LIB_PATH):
+        from dsa_sparse_attention_topk_gb300 import build
+        build.build()
+    return dsa
+
+
+class DeviceWorkload:
+    """A workload's caches and query tensors on the GPU, filled by the library's cache
+    writers from the generator's bf16 rows."""
+
+    def __init__(self, wl, device="cuda", with_kv=True):
+        import dsa_sparse_attention_topk_gb300 as dsa
+        self.wl = wl
+        self.dev = device
+        self.k_cache = dsa.alloc_k_cache(wl.num_pages, device)
+        self.kv_cache = dsa.alloc_kv_cache(wl.num_pages, device) if with_kv else None
+        self.q_idx_cpu = wl.q_index()
+        self.w_cpu = wl.weights()
+        for b in range(wl.B):
+            slots = torch.from_numpy(wl.slot_mapping(b)).to(device)
+            k = wl.k_seq(b, self.q_idx_cpu, self.w_cpu).to(device)
+            dsa.quant_kv_mxfp8(k, slots, self.k_cache)
+            if with_kv:
+                kv = wl.kv_seq(b).to(device)
+                dsa.quant_kv_fp8(kv, slots, self.kv_cache)
+        self.page_table = torch.from_numpy(wl.page_table).to(device)
+        self.seq_lens = torch.from_numpy(wl.seq_lens).to(device)
+        self.q_seq = torch.from_numpy(wl.q_seq).to(device)
+        self.q_pos = torch.from_numpy(wl.q_pos).to(device)
+        self.q_idx = self.q_idx_cpu.to(device)
+        self.w = self.w_cpu.to(device)
+        self._q_sfa = None
+
+    @property
+    def q_sfa(self):
+        if self._q_sfa is None:
+            self._q_sfa = self.wl.q_sfa().to(self.dev)
+        return self._q_sfa
+
+    def indexer_topk(self, with_scores=True):
+        import dsa_sparse_attention_topk_gb300 as dsa
+        wl = self.wl
+        sc = torch.empty(wl.n_q, wl.topk, dtype=torch.float32, device=self.dev) if with_scores else None
+        idx, sc = dsa.indexer_topk(self.q_idx, self.w, self.k_cache, self.page_table, self.seq_lens,
+                                   self.q_seq, self.q_pos, wl.topk, wl.max_ctx, q_group=wl.q_group,
+                                   out_scores=sc)
+        return idx, sc
+
+    def indexer_scores(self):
+        import dsa_sparse_attention_topk_gb300 as dsa
+        wl = self.wl
+        return dsa.indexer_scores(self.q_idx, self.w, self.k_cache, self.page_table, self.seq_lens,
+                                  self.q_seq, self.q_pos, wl.max_ctx, q_group=wl.q_group)
+
+    def sparse_attn(self, idx, with_lse=True):
+        import dsa_sparse_attention_topk_gb300 as dsa
+        wl = self.wl
+        lse = torch.empty(wl.n_q, wl.h_s, dtype=torch.float32, device=self.dev) if with_lse else None
+        return dsa.sparse_attn(self.q_sfa, self.kv_cache, self.page_table, self.seq_lens, self.q_seq,
+                               idx, wl.sm_scale, out_lse=lse)
+
+
+class OracleRows:
+    """Oracle evaluation of chosen query rows of a workload (regenerating only the
+    sequences those rows need)."""
+
+    def __init__(self, wl):
+        self.wl = wl
+        self.q_idx = wl.q_index().double().numpy()
+        self.w = wl.weights().double().numpy()
+        self._k = {}
+        self._kv = {}
+
+    def k_hat(self, b):
+        if b not in self._k:
+            k = self.wl.k_seq(b).double().numpy()
+            c, s = oracle.mxfp8_quantize(k)
+            self._k[b] = oracle.mxfp8_dequantize(c, s)
+        return self._k[b]
+
+    def kv_hat_rows(self, b, rows_idx):
+        """Dequantised latent rows of sequence b at positions rows_idx (others zero)."""
+        if b not in self._kv:
+            self._kv[b] = self.wl.kv_seq(b).double().numpy()
+        kv = self._kv[b]
+        out = np.zeros_like(kv)
+        sel = np.unique(rows_idx[rows_idx >= 0])
+        if sel.size:
+            c, s = oracle.fp8_tile_quantize(kv[sel])
+            out[sel] = oracle.fp8_tile_dequantize(c, s)
+        return out
+
+    def q_hat(self, r):
+        c, s = oracle.mxfp8_quantize(self.q_idx[r])
+        return oracle.mxfp8_dequantize(c, s)
+
+    def n_sel(self, r):
+        wl = self.wl
+        return selectable_count(wl.q_pos[r], wl.seq_lens[wl.q_seq[r]])
+
+    def scores(self, r):
+        b = int(self.wl.q_seq[r])
+        n = self.n_sel(r)
+        kh = self.k_hat(b)[:n]
+        qh = self.q_hat(r)
+        return oracle.indexer_scores_row(qh, self.w[r], kh), indexer_magnitude_row(qh, self.w[r], kh)
+
+    def topk(self, r):
+        s, mag = self.scores(r)
+        idx, vals = oracle.topk_row(s, self.wl.topk)
+        return idx, s, mag
+
+    def sfa(self, r, idx, q_sfa_row):
+        b = int(self.wl.q_seq[r])
+        kvh = self.kv_hat_rows(b, np.asarray(idx))
+        return oracle.sparse_attention_row(q_sfa_row, kvh, np.asarray(idx), self.wl.sm_scale)
+
+
+def check_scores(gpu_row, ref, mag, n):
+    """Full score row from dsa_indexer_scores vs the oracle."""
+    g = np.asarray(gpu_row, np.float64)
+    assert np.all(np.isneginf(g[n:])), "non-selectable positions must be -inf"
+    err = np.abs(g[:n] - ref)
+    tol = SCORE_RTOL * np.maximum(np.abs(ref), mag)
+    bad = np.nonzero(err > tol)[0]
+    assert bad.size == 0, f"{bad.size} scores out of tolerance, first at {bad[:5]}: gpu {g[bad[:5]]} ref {ref[bad[:5]]}"
+
+
+def check_topk(gpu_idx, gpu_vals, ref_s, mag, k):
+    """Top-K set parity with the tie band; gpu_vals (if given) must match the oracle
+    scores of the returned positions."""
+    gi = np.asarray(gpu_idx)
+    n = ref_s.shape[0]
+    m = min(k, n)
+    sel = gi[gi >= 0]
+    assert np.all(gi[gi < 0] == -1), "padding must be -1"
+    assert sel.size == m, f"selected {sel.size}, want {m}"
+    assert np.unique(sel).size == sel.size, "duplicate indices"
+    assert sel.min() >= 0 and sel.max() < n, "index outside the selectable range"
+    if n <= k:
+        assert np.array_equal(np.sort(sel), np.arange(n))
+        return
+    order = np.argsort(-ref_s, kind="stable")
+    ref_set = set(order[:k].tolist())
+    kth = ref_s[order[k - 1]]
+    band = SCORE_RTOL * max(abs(kth), mag[order[k - 1]])
+    diff = ref_set.symmetric_difference(set(sel.tolist()))
+    out_band = [p for p in diff if abs(ref_s[p] - kth) > band]
+    assert not out_band, f"{len(out_band)} positions differ outside the tie band (first {out_band[:5]})"
+    if gpu_vals is not None:
+        gv = np.asarray(gpu_vals, np.float64)[gi >= 0]
+        err = np.abs(gv - ref_s[sel])
+        tol = SCORE_RTOL * np.maximum(np.abs(ref_s[sel]), mag[sel])
+        assert np.all(err <= tol), "returned scores out of tolerance"
+    return len(diff)
+
+
+def check_sfa(gpu_o, ref_o):
+    g = np.asarray(gpu_o, np.float64)
+    d = np.abs(g - ref_o)
+    assert d.max() <= SFA_MAX_ABS, f"max-abs {d.max():.3e}"
+    assert d.mean() <= SFA_MEAN_ABS, f"mean-abs {d.mean():.3e}"
+    return d.max(), d.mean()

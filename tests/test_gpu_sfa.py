@@ -1,0 +1,97 @@
+"""GPU parity of Sparse Flash Attention against the float64 oracle (max-abs 2e-2,
+mean-abs 2e-3 on the bf16 output; lse within 1e-3), fed with the oracle's own Top-K
+indices, plus padding, empty rows, out-of-range indices and fewer heads."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from dsa_sparse_attention_topk_gb300 import workloads as W
+from dsa_testlib import ensure_built, DeviceWorkload, OracleRows, check_sfa
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    return ensure_built()
+
+
+def _oracle_idx(orc, wl):
+    return np.stack([orc.topk(r)[0] for r in range(wl.n_q)]).astype(np.int32)
+
+
+CASES = {
+    "tiny": lambda: W.make("tiny"),
+    "short_ctx": lambda: W.make("short_ctx"),
+    "ragged_h100": lambda: W.custom([300, 1, 2500, 129], h_i=16, h_s=100, topk=256, seed=17),
+    "mtp_h128": lambda: W.custom([1500, 700], per_seq=2, h_i=16, h_s=128, topk=512, seed=18),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_sfa_matches_oracle(dsa, name):
+    wl = CASES[name]()
+    dw = DeviceWorkload(wl)
+    orc = OracleRows(wl)
+    idx = _oracle_idx(orc, wl)
+    out, lse = dw.sparse_attn(torch.from_numpy(idx).cuda())
+    assert dsa.device_status() == 0
+    out = out.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    qs = wl.q_sfa().double().numpy()
+    for r in range(wl.n_q):
+        o_ref, lse_ref = orc.sfa(r, idx[r], qs[r])
+        check_sfa(out[r], o_ref)
+        assert np.allclose(lse[r], lse_ref, rtol=1e-3, atol=1e-3)
+
+
+def test_sfa_padding_order_empty_and_bad_index(dsa):
+    wl = W.custom([400, 90], h_i=8, h_s=32, topk=64, seed=19)
+    dw = DeviceWorkload(wl)
+    orc = OracleRows(wl)
+    rng = np.random.default_rng(3)
+    idx = np.full((2, 64), -1, np.int32)
+    idx[0, 5:45] = rng.choice(400, 40, replace=False)      # padding on both sides
+    out, lse = dw.sparse_attn(torch.from_numpy(idx).cuda())
+    assert dsa.device_status() == 0
+    qs = wl.q_sfa().double().numpy()
+    o_ref, _ = orc.sfa(0, idx[0], qs[0])
+    check_sfa(out[0].float().cpu().numpy(), o_ref)
+    # row 1 is empty: zeros and -inf
+    assert not out[1].float().abs().sum().item()
+    assert torch.all(torch.isneginf(lse[1]))
+    # reversing the index order changes nothing beyond rounding
+    idx2 = idx.copy()
+    idx2[0] = idx[0][::-1]
+    out2, _ = dw.sparse_attn(torch.from_numpy(idx2).cuda())
+    assert (out2[0].float() - out[0].float()).abs().max().item() <= 1e-2
+    # an index past the sequence end is skipped and flagged
+    idx3 = idx.copy()
+    idx3[1, 0] = 90
+    out3, _ = dw.sparse_attn(torch.from_numpy(idx3).cuda())
+    assert dsa.device_status() & 8
+    assert not out3[1].float().abs().sum().item()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["decode_b32_ctx32k", "long_mtp_b4_ctx128k"])
+def test_sfa_full_size_sampled(dsa, name):
+    wl = W.make(name)
+    dw = DeviceWorkload(wl)
+    orc = OracleRows(wl)
+    gpu_idx, _ = dw.indexer_topk(with_scores=False)
+    idx = gpu_idx.cpu().numpy().copy()
+    rows = [0, wl.n_q - 1]
+    for r in rows:                      # sampled rows get the oracle's own selection
+        idx[r] = orc.topk(r)[0]
+    out, lse = dw.sparse_attn(torch.from_numpy(idx).cuda())
+    assert dsa.device_status() == 0
+    out = out.float().cpu().numpy()
+    qs = wl.q_sfa(rows).double().numpy()
+    for i, r in enumerate(rows):
+        o_ref, lse_ref = orc.sfa(r, idx[r], qs[i])
+        check_sfa(out[r], o_ref)
+        assert np.allclose(lse.cpu().numpy()[r], lse_ref, rtol=1e-3, atol=1e-3)
