@@ -42,7 +42,7 @@ struct IdxSmemHead {
 // Dynamic shared memory: [IdxSmemHead][w: G*H floats][q_hat: G*H*128 floats][keys: G*chunk_cap]
 __host__ __device__ inline size_t idx_smem_bytes(int G, int H, int chunk_cap) {
   size_t head = (sizeof(IdxSmemHead) + 15) & ~size_t(15);
-  return head + sizeof(float) * G * H + sizeof(float) * G * H * kIdxDim +
+  return head + sizeof(float) * ((G * H + 3) & ~3) + sizeof(float) * G * H * kIdxDim +
          sizeof(uint32_t) * size_t(G) * chunk_cap;
 }
 
@@ -79,7 +79,7 @@ indexer_cuda_core_kernel(IndexerArgs a, int chunk_cap) {
   const size_t head = (sizeof(IdxSmemHead) + 15) & ~size_t(15);
   const int H = a.h_i;
   float* s_w = reinterpret_cast<float*>(smem_raw + head);
-  float* s_q = s_w + G * H;
+  float* s_q = s_w + ((G * H + 3) & ~3);  // 16-byte aligned for the float4 stores
   uint32_t* s_keys = reinterpret_cast<uint32_t*>(s_q + G * H * kIdxDim);
 
   const int tid = threadIdx.x;

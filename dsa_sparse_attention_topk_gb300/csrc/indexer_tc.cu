@@ -1,0 +1,455 @@
+// Fused Lightning Indexer + Top-K on the 5th-generation tensor cores.
+//
+// "Deep Dive into Sparse Attention and Engineering Optimizations for Efficient Inference
+// in Kimi K3.1 Pro", section 2.1, and "Kimi K3.1 Pro Inference Acceleration: Day0
+// Optimization on Heterogeneous AI Hardware", section "Lightning Indexer Three-Stream
+// Coordination": scoring, head-weight weighting and Top-K selection run in one kernel
+// reading the paged K-cache directly, with Top-K pipelined behind the K-cache reads; the
+// section "Full MXFP8 Quantization with Per-Group Dynamic Scaling for LI" gives the
+// operand format (E4M3, one scale per 32 elements).
+//
+//   score[t, p] = sum_h w[t, h] * max(0, q_hat[t, h] . k_hat[p])
+//
+// One thread-block cluster of C CTAs handles a group of G query rows of one sequence;
+// CTA r owns the r-th chunk (a multiple of 128 positions) of the positions the group may
+// select.  Inside a CTA, warps specialise:
+//   warp 0     producer: per 128-position tile, two TMA loads of 64x128 E4M3 page rows
+//              (128-byte swizzle) and two 256-byte bulk loads of the pages' E8M0 scales
+//              into an S-stage shared-memory ring;
+//   warp 1     MMA: transposes the tile's scales into the tcgen05 scale-factor layout,
+//              copies them to TMEM and issues four block-scaled MXFP8 MMAs
+//              (M = 128 positions, N = G * Hp query heads, K = 4 x 32) into a
+//              double-buffered TMEM accumulator;
+//   warps 2-5  epilogue: one TMEM lane (= one position) per thread, ReLU, head weights and
+//              the sum over heads in registers, then the score's order-preserving key goes
+//              to shared memory.  No score leaves the chip.
+// The MXFP8 queries are quantised on chip into the MMA's B operand at kernel start.  After
+// the scan, the cluster selects the Top-K of every row over distributed shared memory
+// (topk_cluster.cuh).
+
+#include <algorithm>
+#include <cfloat>
+#include <cuda.h>
+
+#include "dsa_common.cuh"
+#include "dsa_launch.h"
+#include "tc_utils.cuh"
+#include "topk_cluster.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kThreads = 192;          // 6 warps
+constexpr int kTileP = 128;            // positions per MMA tile = two pages
+constexpr int kStageA = kTileP * kIdxDim;        // 16384 B of E4M3 codes
+constexpr int kStageSF = kTileP * 4;             // 512 B of E8M0 scales (position order)
+constexpr int kStageBytes = kStageA + 2 * kStageSF;  // + transposed copy: 17408 = 17 KB
+constexpr int kMaxCluster = 16;
+constexpr int kMaxStages = 8;
+
+struct Plan {
+  int G, H, Hp, Np, nacc, stages, chunk_cap;
+  uint32_t tmem_cols, d_col[2], sfa_col[2], sfb_col;
+  // dynamic shared memory offsets (from a 1024-byte aligned base)
+  uint32_t off_stage, off_b, off_sfb, off_w, off_keys, off_topk, off_bar, total;
+};
+
+struct Barriers {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint32_t tmem_base;
+  int abort;
+  int seq;
+  int n_max;
+  int n_sel[4];
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+__host__ inline Plan make_plan(int G, int H, int chunk_cap, int stages) {
+  Plan p{};
+  p.G = G;
+  p.H = H;
+  p.Hp = (H + 15) / 16 * 16;
+  p.Np = G * p.Hp;
+  p.nacc = p.Np <= 128 ? 2 : 1;
+  p.stages = stages;
+  p.chunk_cap = chunk_cap;
+  uint32_t used = p.nacc * p.Np + 16;
+  uint32_t cols = 32;
+  while (cols < used) cols *= 2;
+  p.tmem_cols = cols;
+  p.d_col[0] = 0;
+  p.d_col[1] = p.Np;
+  p.sfa_col[0] = p.nacc * p.Np;
+  p.sfa_col[1] = p.nacc * p.Np + 4;
+  p.sfb_col = p.nacc * p.Np + 8;
+  uint32_t o = 0;
+  p.off_stage = o; o += stages * kStageBytes;
+  p.off_b = o = align_up(o, 1024); o += p.Np * kIdxDim;
+  p.off_sfb = o = align_up(o, 16); o += 2 * 512;
+  p.off_w = o; o += 4 * G * p.Hp;
+  p.off_keys = o = align_up(o, 16); o += 4u * G * chunk_cap;
+  p.off_topk = o = align_up(o, 16); o += sizeof(TopkSmem);
+  p.off_bar = o = align_up(o, 16); o += sizeof(Barriers);
+  p.total = o;
+  return p;
+}
+
+// MXFP8-quantise one 128-wide bf16 row straight into the B operand (128-byte swizzled
+// K-major row n) and return this lane's group exponent code (lanes 0, 8, 16, 24 hold
+// groups 0..3).  Same OCP MX rule as the cache writer.
+__device__ __forceinline__ uint32_t quant_row_to_b(const __nv_bfloat16* src, uint8_t* b_row_base, int n) {
+  const int lane = threadIdx.x & 31;
+  const uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+  float x[4] = {__low2float(a), __high2float(a), __low2float(b), __high2float(b)};
+  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const int e = mx_shared_exp(amax);
+  const float inv = exp2i(-e);
+  uint32_t codes = 0;
+  if (amax > 0.f)
+    codes = static_cast<uint32_t>(f32x2_to_e4m3x2(x[0] * inv, x[1] * inv)) |
+            (static_cast<uint32_t>(f32x2_to_e4m3x2(x[2] * inv, x[3] * inv)) << 16);
+  const int chunk = lane >> 2;  // 16-byte chunk of the 128-byte row
+  *reinterpret_cast<uint32_t*>(b_row_base + n * 128 + ((chunk ^ (n & 7)) << 4) + (lane & 3) * 4) = codes;
+  return static_cast<uint32_t>(e + 127);
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1)
+indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan pl) {
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  Barriers& bs = *reinterpret_cast<Barriers*>(smem + pl.off_bar);
+  TopkSmem& tk = *reinterpret_cast<TopkSmem*>(smem + pl.off_topk);
+  uint8_t* s_b = smem + pl.off_b;
+  uint32_t* s_sfb = reinterpret_cast<uint32_t*>(smem + pl.off_sfb);
+  float* s_w = reinterpret_cast<float*>(smem + pl.off_w);
+  uint32_t* s_keys = reinterpret_cast<uint32_t*>(smem + pl.off_keys);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int C = static_cast<int>(cluster_nctarank());
+  const int row0 = blockIdx.y * G;
+  const int H = pl.H, Hp = pl.Hp, Np = pl.Np, S = pl.stages;
+
+  // ---- prologue -------------------------------------------------------------------
+  topk_init(tk);
+  if (tid == 0) {
+    int seq = a.q_seq[row0];
+    unsigned bad = 0;
+    if (seq < 0 || seq >= a.n_seq) { bad |= DSA_STATUS_BAD_SEQ; seq = -1; }
+    int L = 0;
+    if (seq >= 0) {
+      L = a.seq_lens[seq];
+      if (L < 0 || L > a.max_ctx) { bad |= DSA_STATUS_BAD_LEN; L = L < 0 ? 0 : a.max_ctx; }
+    }
+    int n_max = 0;
+    for (int j = 0; j < G; ++j) {
+      if (a.q_seq[row0 + j] != a.q_seq[row0]) bad |= DSA_STATUS_BAD_SEQ;
+      long long n = static_cast<long long>(a.q_pos[row0 + j]) + 1;
+      n = n < 0 ? 0 : (n > L ? L : n);
+      bs.n_sel[j] = static_cast<int>(n);
+      n_max = n > n_max ? static_cast<int>(n) : n_max;
+    }
+    bs.seq = seq;
+    bs.n_max = n_max;
+    bs.abort = 0;
+    if (bad && rank == 0) flag(a.status, bad);
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(&bs.full[s], 1);
+      tc::mbar_init(&bs.empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&bs.tfull[i], 1);
+      tc::mbar_init(&bs.tempty[i], 128);
+    }
+    tc::mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) tc::prefetch_tmap(&kmap);
+  // B operand: on-chip MXFP8 quantisation of the group's queries (row n = j * Hp + h)
+  for (int n = warp; n < Np; n += kThreads / 32) {
+    const int j = n / Hp, h = n % Hp;
+    uint32_t ecode = 127;
+    if (h < H) {
+      ecode = quant_row_to_b(static_cast<const __nv_bfloat16*>(a.q) + (static_cast<size_t>(row0 + j) * H + h) * kIdxDim,
+                             s_b, n);
+    } else {
+      const int chunk = lane >> 2;
+      *reinterpret_cast<uint32_t*>(s_b + n * 128 + ((chunk ^ (n & 7)) << 4) + (lane & 3) * 4) = 0u;
+    }
+    // gather the four group codes (lanes 0, 8, 16, 24) into one scale word
+    const uint32_t e1 = __shfl_sync(0xffffffffu, ecode, 8), e2 = __shfl_sync(0xffffffffu, ecode, 16),
+                   e3 = __shfl_sync(0xffffffffu, ecode, 24);
+    if (lane == 0) {
+      const uint32_t word = ecode | (e1 << 8) | (e2 << 16) | (e3 << 24);
+      // scale-factor layout: block n/128, row n%32, word (n/32)%4
+      s_sfb[(n >> 7) * 128 + (n & 31) * 4 + ((n >> 5) & 3)] = word;
+    }
+  }
+  // scale words of padding rows up to the end of the last 128-row block
+  for (int n = Np + tid; n < ((Np + 127) / 128) * 128; n += kThreads)
+    s_sfb[(n >> 7) * 128 + (n & 31) * 4 + ((n >> 5) & 3)] = 0x7F7F7F7Fu;
+  for (int i = tid; i < G * Hp; i += kThreads) {
+    const int j = i / Hp, h = i % Hp;
+    s_w[i] = h < H ? a.w[static_cast<size_t>(row0 + j) * H + h] : 0.f;
+  }
+  if (warp == 1) tc::tmem_alloc(&bs.tmem_base, pl.tmem_cols);
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // every CTA of the cluster initialised before any DSMEM traffic
+  tc::fence_after_sync();
+
+  const int seq = bs.seq;
+  const int n_max = bs.n_max;
+  int chunk = (n_max + C - 1) / C;
+  chunk = (chunk + kTileP - 1) / kTileP * kTileP;
+  if (chunk > pl.chunk_cap) chunk = pl.chunk_cap;
+  const int c0 = rank * chunk;
+  const int len = max(0, min(chunk, n_max - c0));
+  const int ntiles = (len + kTileP - 1) / kTileP;
+  const int n_pages_needed = (n_max + kPage - 1) / kPage;
+  const int32_t* ptab = a.page_table + static_cast<size_t>(seq < 0 ? 0 : seq) * a.max_pages;
+  const uint32_t tmem = bs.tmem_base;
+  volatile int* abort = &bs.abort;
+
+  auto phys_page = [&](int lp) -> int {
+    if (seq < 0 || lp >= n_pages_needed || lp >= a.max_pages) return -1;
+    const int pg = ptab[lp];
+    return (pg >= 0 && pg < a.num_pages) ? pg : -2;
+  };
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % S, it = t / S;
+        tc::mbar_wait(&bs.empty[s], (it & 1) ^ 1, abort, a.status);
+        uint8_t* st = smem + pl.off_stage + s * kStageBytes;
+        const int lp = (c0 + t * kTileP) / kPage;
+        const int pg0 = phys_page(lp), pg1 = phys_page(lp + 1);
+        if (pg0 == -2 || pg1 == -2) flag(a.status, DSA_STATUS_BAD_PAGE);
+        const uint32_t bytes = (pg0 >= 0 ? (kKPageBytes) : 0) + (pg1 >= 0 ? (kKPageBytes) : 0);
+        tc::mbar_arrive_expect_tx(&bs.full[s], bytes);
+        if (pg0 >= 0) {
+          tc::tma_load_3d(st, &kmap, 0, 0, pg0, &bs.full[s]);
+          tc::bulk_load(st + kStageA, a.k_cache + static_cast<int64_t>(pg0) * kKPageBytes + kKScaleOff, 256,
+                        &bs.full[s]);
+        }
+        if (pg1 >= 0) {
+          tc::tma_load_3d(st + kStageA / 2, &kmap, 0, 0, pg1, &bs.full[s]);
+          tc::bulk_load(st + kStageA + 256, a.k_cache + static_cast<int64_t>(pg1) * kKPageBytes + kKScaleOff, 256,
+                        &bs.full[s]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      tc::cp_32x128b_warpx4(tmem + pl.sfb_col, tc::desc_sf_block(smem_u32(s_sfb)));
+      if (Np > 128) tc::cp_32x128b_warpx4(tmem + pl.sfb_col + 4, tc::desc_sf_block(smem_u32(s_sfb + 128)));
+    }
+    const uint64_t bdesc = tc::desc_kmajor_sw128(smem_u32(s_b));
+    for (int t = 0; t < ntiles; ++t) {
+      const int s = t % S, it = t / S;
+      const int acc = t % pl.nacc, ia = t / pl.nacc;
+      uint8_t* st = smem + pl.off_stage + s * kStageBytes;
+      tc::mbar_wait(&bs.full[s], it & 1, abort, a.status);
+      // scales: position order -> [32 rows][4 words], word (i, j) = position 32 j + i
+      const uint32_t* sf_nat = reinterpret_cast<const uint32_t*>(st + kStageA);
+      uint32_t* sf_t = reinterpret_cast<uint32_t*>(st + kStageA + kStageSF);
+      const uint4 v = make_uint4(sf_nat[lane], sf_nat[32 + lane], sf_nat[64 + lane], sf_nat[96 + lane]);
+      *reinterpret_cast<uint4*>(sf_t + 4 * lane) = v;
+      tc::fence_async_smem();
+      __syncwarp();
+      tc::mbar_wait(&bs.tempty[acc], (ia & 1) ^ 1, abort, a.status);
+      tc::fence_after_sync();
+      if (lane == 0) {
+        const uint32_t d = tmem + pl.d_col[acc];
+        const uint32_t sfa = tmem + pl.sfa_col[acc];
+        tc::cp_32x128b_warpx4(sfa, tc::desc_sf_block(smem_u32(sf_t)));
+        const uint64_t adesc = tc::desc_kmajor_sw128(smem_u32(st));
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_mxf8(d, adesc + 2 * k, bdesc + 2 * k, tc::idesc_mxf8_e4m3(Np, k), sfa, tmem + pl.sfb_col, k > 0);
+        tc::commit(&bs.empty[s]);
+        tc::commit(&bs.tfull[acc]);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
+    const int m = quarter * 32 + lane;         // tile row = position offset in the tile
+    for (int t = 0; t < ntiles; ++t) {
+      const int acc = t % pl.nacc, ia = t / pl.nacc;
+      const bool ok = tc::mbar_wait(&bs.tfull[acc], ia & 1, abort, a.status);
+      tc::fence_after_sync();
+      const int local = t * kTileP + m;
+      const int p = c0 + local;
+      const bool page_ok = phys_page(p / kPage) >= 0;
+      float sc[G];
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        float s = 0.f;
+        for (int h0 = 0; h0 < Hp; h0 += 16) {
+          uint32_t r[16];
+          tc::tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + pl.d_col[acc] + j * Hp + h0, r);
+          tc::tmem_wait_ld();
+          const float* wj = s_w + j * Hp + h0;
+#pragma unroll
+          for (int h = 0; h < 16; ++h) s = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.f), s);
+        }
+        sc[j] = s;
+      }
+      tc::fence_before_sync();
+      tc::mbar_arrive(&bs.tempty[acc]);
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const bool valid = ok && page_ok && local < len && p < bs.n_sel[j];
+        s_keys[j * pl.chunk_cap + local] = valid ? score_key(sc[j]) : 0u;
+        if (a.out_full && valid) a.out_full[static_cast<size_t>(row0 + j) * a.max_ctx + p] = sc[j];
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+
+  if (a.out_idx) {
+#pragma unroll 1
+    for (int j = 0; j < G; ++j) {
+      const size_t row = static_cast<size_t>(row0 + j);
+      cluster_topk_row(tk, s_keys + j * pl.chunk_cap, c0, len, bs.n_sel[j], a.topk, a.out_idx + row * a.topk,
+                       a.out_scores ? a.out_scores + row * a.topk : nullptr);
+    }
+  }
+  cluster_sync();  // no CTA leaves while its shared memory may still be addressed
+  tc::fence_after_sync();
+  if (warp == 1) tc::tmem_dealloc(tmem, pl.tmem_cols);
+}
+
+__global__ void fill_kernel(float* p, size_t n, float v) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    p[i] = v;
+}
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
+
+struct DevInfo {
+  int n_sm = 0, smem_optin = 0;
+};
+DevInfo dev_info() {
+  static DevInfo cache[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  DevInfo& d = cache[dev & 63];
+  if (!d.n_sm) {
+    cudaDeviceGetAttribute(&d.n_sm, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  }
+  return d;
+}
+
+template <int G>
+cudaError_t launch_g(const IndexerArgs& a, cudaStream_t s, const char** err) {
+  const DevInfo di = dev_info();
+  const int n_groups = a.n_q / G;
+  const size_t limit = static_cast<size_t>(di.smem_optin) - 1024;  // room for the 1024-byte alignment
+  auto cap_for = [&](int c) {
+    int chunk = (a.max_ctx + c - 1) / c;
+    return (chunk + kTileP - 1) / kTileP * kTileP;
+  };
+  // smallest power-of-two cluster whose score buffer fits next to a 4-stage ring, then
+  // widen while the grid still fits on the GPU in one wave
+  int C = 1;
+  while (C < kMaxCluster && make_plan(G, a.h_i, cap_for(C), 4).total > limit) C *= 2;
+  while (C < kMaxCluster && static_cast<long long>(n_groups) * C * 2 <= di.n_sm) C *= 2;
+  int stages = kMaxStages;
+  while (stages > 2 && make_plan(G, a.h_i, cap_for(C), stages).total > limit) --stages;
+  const Plan pl = make_plan(G, a.h_i, cap_for(C), stages);
+  if (pl.total > limit) {
+    *err = "indexer: max_ctx too large for the on-chip score buffer";
+    return cudaErrorInvalidValue;
+  }
+  // at least ~120 KB so that one CTA (and one TMEM allocation) owns each SM
+  const size_t smem = std::max<size_t>(pl.total + 1024, 120 * 1024);
+
+  EncodeFn enc = encode_fn();
+  if (!enc) {
+    *err = "indexer: cuTensorMapEncodeTiled is not available";
+    return cudaErrorNotSupported;
+  }
+  CUtensorMap map;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kIdxDim), static_cast<cuuint64_t>(kPage),
+                              static_cast<cuuint64_t>(a.num_pages)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kIdxDim), static_cast<cuuint64_t>(kKPageBytes)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kIdxDim), static_cast<cuuint32_t>(kPage), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.k_cache), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+    *err = "indexer: tensor map encoding failed";
+    return cudaErrorInvalidValue;
+  }
+  auto kern = indexer_tc_kernel<G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  if (C > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.out_full) {
+    const size_t n = static_cast<size_t>(a.n_q) * a.max_ctx;
+    fill_kernel<<<1024, 256, 0, s>>>(a.out_full, n, -INFINITY);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, n_groups, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, map, a, pl);
+}
+
+}  // namespace
+
+cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s, const char** err) {
+  if (a.n_q == 0) return cudaSuccess;
+  switch (a.q_group) {
+    case 1: return launch_g<1>(a, s, err);
+    case 2: return launch_g<2>(a, s, err);
+    case 3: return launch_g<3>(a, s, err);
+    case 4: return launch_g<4>(a, s, err);
+    default: *err = "indexer: q_group must be 1..4"; return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dsa

@@ -1,0 +1,491 @@
+// Sparse Flash Attention on the 5th-generation tensor cores.
+//
+// "Deep Dive into Sparse Attention and Engineering Optimizations for Efficient Inference
+// in Kimi K3.1 Pro", section 1 (attention only over the selected positions) and "Adapting
+// and Optimizing Kimi K3.1 Pro for Long-Sequence Inference", section 2 (the cache entries
+// named by the indexer's indices are gathered directly); "Kimi K3.1 Pro Inference
+// Acceleration: Day0 Optimization on Heterogeneous AI Hardware", sections "FP8 KVCache
+// with Per-Token-Head-Tile Quantization for SFA" (FP8 codes with a scale per 128-element
+// tile) and "Preserving a Mixed-Precision Path" (BF16 query and attention weighting).
+//
+// Absorbed MLA decode: each selected position j gives one dequantised latent row kv[j]
+// (576 wide); it is the key and kv[j][0:512] is the value.
+//
+// One CTA handles one query row and one contiguous share ("split") of its selected
+// entries, for all heads at once (M = 128 rows of the MMAs; rows >= h_s are zero):
+//   warp 0      MMA issuer: Q (bf16, 128 x 576, resident, loaded once by TMA) times the
+//               gathered tile (32 entries x 576) -> S in TMEM; then P (bf16) times the
+//               tile's first 512 columns -> O.
+//   warps 1-4   softmax: one head per thread; online softmax in the exp2 domain with a
+//               lazily updated running max (the accumulator is rescaled only when the max
+//               grows by more than 2^8), P written to shared memory as bf16.
+//   warps 5-11  gather: index -> page -> record, 16-byte loads of E4M3 codes, multiply by
+//               the tile scale, bf16 into the 128-byte-swizzled operand tile (double
+//               buffered).  Invalid entries (-1, or past the sequence) become zero rows.
+// TMEM (512 columns): O[:, 0:448] accumulates in columns 0..447.  Columns 448..511 are
+// shared by the S tile (32 columns) and the tile's P V[:, 448:512] product, which the
+// softmax warps add into register accumulators (so the whole 128 x 512 output fits next
+// to the S tile).
+// Several splits of a row write unnormalised partial outputs with their running max and
+// sum to the workspace; a small kernel merges them (log-sum-exp weights).
+
+#include <algorithm>
+#include <cfloat>
+#include <cuda.h>
+
+#include "dsa_common.cuh"
+#include "dsa_launch.h"
+#include "tc_utils.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kTok = 32;                       // selected entries per tile
+constexpr int kSoftWarps = 4;
+constexpr int kGatherWarps = 7;
+constexpr int kThreads = 32 * (1 + kSoftWarps + kGatherWarps);  // 384
+constexpr int kQBlock = 128 * 128;             // one 64-column K-block of Q: 128 rows x 128 B
+constexpr int kQBytes = 9 * kQBlock;           // 147456
+constexpr int kKvBlock = kTok * 128;           // one 64-column K-block of a tile: 4096 B
+constexpr int kKvBytes = 9 * kKvBlock;         // 36864
+constexpr int kPBytes = 128 * kTok * 2;        // 8192
+constexpr uint32_t kColS = 448;                // S tile / tail product columns
+constexpr int kVLeft = 448;                    // output columns accumulated in TMEM
+constexpr int kVTail = 64;                     // output columns accumulated in registers
+constexpr int kChunks = kLatent / 16;          // 16-byte code chunks per entry (36)
+constexpr int kSplitTarget = 148;              // CTAs the split count aims for
+constexpr int kMaxSplit = 16;
+constexpr float kRescaleLog2 = 8.0f;           // lazy max update threshold (factor 256)
+
+struct Ctl {
+  uint64_t q_full;
+  uint64_t kv_full[2];
+  uint64_t kv_empty[2];
+  uint64_t s_full;
+  uint64_t p_full;
+  uint64_t pv_done;
+  uint64_t s_free;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffKv = kQBytes;
+constexpr uint32_t kOffP = kOffKv + 2 * kKvBytes;
+constexpr uint32_t kOffCtl = kOffP + kPBytes;
+constexpr uint32_t kSmemBytes = kOffCtl + 128 + 1024;  // + slack for the 1024-byte alignment
+
+__host__ __device__ inline int split_count(int n_q, int topk) {
+  const int tiles = (topk + kTok - 1) / kTok;
+  int s = kSplitTarget / (n_q > 0 ? n_q : 1);
+  s = s < 1 ? 1 : s;
+  s = s > kMaxSplit ? kMaxSplit : s;
+  return s > tiles ? tiles : s;
+}
+
+struct SfaPlan {
+  int nsplit, tiles_total;
+  float* ws_o;    // [n_q][nsplit][h_s][512] unnormalised partial outputs
+  float* ws_ml;   // [n_q][nsplit][h_s][2] running max (log2 domain) and sum
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  uint8_t* s_q = smem + kOffQ;
+  uint8_t* s_kv = smem + kOffKv;
+  uint8_t* s_p = smem + kOffP;
+  Ctl& ctl = *reinterpret_cast<Ctl*>(smem + kOffCtl);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x, t = blockIdx.y;
+  const int tile0 = split * pl.tiles_total / pl.nsplit;
+  const int nt = (split + 1) * pl.tiles_total / pl.nsplit - tile0;
+
+  const int seq = a.q_seq[t];
+  const bool seq_ok = seq >= 0 && seq < a.n_seq;
+  const int L = seq_ok ? a.seq_lens[seq] : 0;
+  const int32_t* ptab = a.page_table + static_cast<size_t>(seq_ok ? seq : 0) * a.max_pages;
+  const int32_t* idx = a.idx + static_cast<size_t>(t) * a.topk;
+
+  if (tid == 0) {
+    if (!seq_ok && split == 0) flag(a.status, DSA_STATUS_BAD_SEQ);
+    ctl.abort = 0;
+    tc::mbar_init(&ctl.q_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&ctl.kv_full[b], kGatherWarps);
+      tc::mbar_init(&ctl.kv_empty[b], 1);
+    }
+    tc::mbar_init(&ctl.s_full, 1);
+    tc::mbar_init(&ctl.p_full, kSoftWarps);
+    tc::mbar_init(&ctl.pv_done, 1);
+    tc::mbar_init(&ctl.s_free, kSoftWarps);
+    tc::mbar_fence_init();
+  }
+  if (warp == 0) tc::tmem_alloc(&ctl.tmem_base, 512);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = ctl.tmem_base;
+  volatile int* abort = &ctl.abort;
+
+  // validity of selected entry e of this row (and its cache record)
+  auto record = [&](int e, bool report) -> const uint8_t* {
+    if (e >= a.topk) return nullptr;
+    const int p = idx[e];
+    if (p < 0) return nullptr;
+    if (p >= L || p / kPage >= a.max_pages) {
+      if (report) flag(a.status, DSA_STATUS_BAD_INDEX);
+      return nullptr;
+    }
+    const int page = ptab[p / kPage];
+    if (page < 0 || page >= a.num_pages) {
+      if (report) flag(a.status, DSA_STATUS_BAD_PAGE);
+      return nullptr;
+    }
+    return a.kv_cache + (static_cast<int64_t>(page) * kPage + p % kPage) * kKvTokBytes;
+  };
+
+  if (warp == 0) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      tc::prefetch_tmap(&qmap);
+      tc::mbar_arrive_expect_tx(&ctl.q_full, kQBytes);
+      for (int kb = 0; kb < 9; ++kb) tc::tma_load_3d(s_q + kb * kQBlock, &qmap, kb * 64, 0, t, &ctl.q_full);
+      tc::mbar_wait(&ctl.q_full, 0, abort, a.status);
+      const uint32_t id_qk = tc::idesc_bf16(kTok, false, false);
+      const uint32_t id_v0 = tc::idesc_bf16(256, false, true);
+      const uint32_t id_v1 = tc::idesc_bf16(192, false, true);
+      const uint32_t id_v2 = tc::idesc_bf16(64, false, true);
+      for (int j = 0; j < nt; ++j) {
+        const int b = j & 1;
+        uint8_t* kv = s_kv + b * kKvBytes;
+        tc::mbar_wait(&ctl.kv_full[b], (j >> 1) & 1, abort, a.status);
+        tc::mbar_wait(&ctl.s_free, (j & 1) ^ 1, abort, a.status);
+        tc::fence_after_sync();
+        for (int kb = 0; kb < 9; ++kb) {
+          const uint64_t qd = tc::desc_kmajor_sw128(smem_u32(s_q + kb * kQBlock));
+          const uint64_t kd = tc::desc_kmajor_sw128(smem_u32(kv + kb * kKvBlock));
+#pragma unroll
+          for (int k = 0; k < 4; ++k) tc::mma_bf16(tmem + kColS, qd + 2 * k, kd + 2 * k, id_qk, (kb | k) != 0);
+        }
+        tc::commit(&ctl.s_full);
+        tc::mbar_wait(&ctl.p_full, j & 1, abort, a.status);
+        tc::fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+          const uint64_t pd = tc::smem_desc(smem_u32(s_p + ks * 256), 128, 512, 0);
+          const uint32_t kofs = ks * 2048;  // 16 entries = two 8-row groups
+          tc::mma_bf16(tmem + 0, pd, tc::smem_desc(smem_u32(kv + 0 * kKvBlock + kofs), kKvBlock, 1024, 2), id_v0,
+                       j > 0 || ks > 0);
+          tc::mma_bf16(tmem + 256, pd, tc::smem_desc(smem_u32(kv + 4 * kKvBlock + kofs), kKvBlock, 1024, 2), id_v1,
+                       j > 0 || ks > 0);
+          tc::mma_bf16(tmem + kColS, pd, tc::smem_desc(smem_u32(kv + 7 * kKvBlock + kofs), kKvBlock, 1024, 2), id_v2,
+                       ks > 0);
+        }
+        tc::commit(&ctl.pv_done);
+        tc::commit(&ctl.kv_empty[b]);
+      }
+    }
+  } else if (warp <= kSoftWarps) {
+    // ---------------- softmax (warps 1..4) ----------------
+    const int quarter = warp & 3;
+    const int m = quarter * 32 + lane;  // head row
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const float c2 = a.sm_scale * 1.4426950408889634f;  // logits in log2 units
+    float m_ref = -INFINITY, l = 0.f;
+    float ot[kVTail];
+#pragma unroll
+    for (int i = 0; i < kVTail; ++i) ot[i] = 0.f;
+    for (int j = 0; j < nt; ++j) {
+      const int e = (tile0 + j) * kTok + lane;
+      const uint32_t mask = __ballot_sync(0xffffffffu, record(e, false) != nullptr);
+      tc::mbar_wait(&ctl.s_full, j & 1, abort, a.status);
+      tc::fence_after_sync();
+      uint32_t sr[32];
+      tc::tmem_ld32(tmem + lane_base + kColS, sr);
+      tc::tmem_wait_ld();
+      float x[32];
+      float mt = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        x[i] = ((mask >> i) & 1u) ? __uint_as_float(sr[i]) * c2 : -INFINITY;
+        mt = fmaxf(mt, x[i]);
+      }
+      const bool need = mt > m_ref + kRescaleLog2 || (m_ref == -INFINITY && mt > -INFINITY);
+      const float m_new = need ? mt : m_ref;
+      const float alpha = need ? exp2f(m_ref - m_new) : 1.f;  // exp2(-inf) = 0
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // rescale the TMEM part of this head's accumulator
+        for (int c = 0; c < kVLeft; c += 16) {
+          uint32_t r[16];
+          tc::tmem_ld16(tmem + lane_base + c, r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tc::tmem_st16(tmem + lane_base + c, r);
+        }
+        tc::tmem_wait_st();
+      }
+#pragma unroll
+      for (int i = 0; i < kVTail; ++i) ot[i] *= alpha;
+      l *= alpha;
+      m_ref = m_new;
+      uint32_t pk[16];
+      float lsum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const float p0 = (m_ref == -INFINITY) ? 0.f : exp2f(x[i] - m_ref);
+        const float p1 = (m_ref == -INFINITY) ? 0.f : exp2f(x[i + 1] - m_ref);
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+        lsum += __low2float(pb) + __high2float(pb);
+        pk[i >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
+      }
+      l += lsum;
+      // P row m: core matrix (m/8, chunk c) at (m/8)*512 + c*128, row offset (m%8)*16
+      uint8_t* prow = s_p + (m >> 3) * 512 + (m & 7) * 16;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(prow + c * 128) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      tc::fence_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&ctl.p_full);
+      tc::mbar_wait(&ctl.pv_done, j & 1, abort, a.status);
+      tc::fence_after_sync();
+#pragma unroll
+      for (int h = 0; h < kVTail; h += 32) {
+        uint32_t r[32];
+        tc::tmem_ld32(tmem + lane_base + kColS + h, r);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ot[h + i] += __uint_as_float(r[i]);
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&ctl.s_free);
+    }
+    // ---- output: final (one split) or partial (several) ----
+    const bool row_ok = m < a.h_s;
+    if (pl.nsplit == 1) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(t) * a.h_s + m) * kVDim;
+      for (int c = 0; c < kVLeft; c += 16) {
+        uint32_t r[16];
+        if (nt > 0) {
+          tc::tmem_ld16(tmem + lane_base + c, r);
+          tc::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) r[i] = 0u;
+        }
+        if (row_ok) {
+          uint4 v0 = make_uint4(pack_bf16(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv),
+                                pack_bf16(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv),
+                                pack_bf16(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv),
+                                pack_bf16(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv));
+          uint4 v1 = make_uint4(pack_bf16(__uint_as_float(r[8]) * inv, __uint_as_float(r[9]) * inv),
+                                pack_bf16(__uint_as_float(r[10]) * inv, __uint_as_float(r[11]) * inv),
+                                pack_bf16(__uint_as_float(r[12]) * inv, __uint_as_float(r[13]) * inv),
+                                pack_bf16(__uint_as_float(r[14]) * inv, __uint_as_float(r[15]) * inv));
+          *reinterpret_cast<uint4*>(out + c) = v0;
+          *reinterpret_cast<uint4*>(out + c + 8) = v1;
+        }
+      }
+      if (row_ok) {
+#pragma unroll
+        for (int c = 0; c < kVTail; c += 8) {
+          *reinterpret_cast<uint4*>(out + kVLeft + c) =
+              make_uint4(pack_bf16(ot[c] * inv, ot[c + 1] * inv), pack_bf16(ot[c + 2] * inv, ot[c + 3] * inv),
+                         pack_bf16(ot[c + 4] * inv, ot[c + 5] * inv), pack_bf16(ot[c + 6] * inv, ot[c + 7] * inv));
+        }
+        if (a.out_lse)
+          a.out_lse[static_cast<size_t>(t) * a.h_s + m] = l > 0.f ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      }
+    } else {
+      const size_t slot = (static_cast<size_t>(t) * pl.nsplit + split) * a.h_s + m;
+      float* wo = pl.ws_o + slot * kVDim;
+      for (int c = 0; c < kVLeft; c += 16) {
+        uint32_t r[16];
+        if (nt > 0) {
+          tc::tmem_ld16(tmem + lane_base + c, r);
+          tc::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) r[i] = 0u;
+        }
+        if (row_ok) {
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<uint4*>(wo + c + i) = make_uint4(r[i], r[i + 1], r[i + 2], r[i + 3]);
+        }
+      }
+      if (row_ok) {
+#pragma unroll
+        for (int c = 0; c < kVTail; c += 4)
+          *reinterpret_cast<float4*>(wo + kVLeft + c) = make_float4(ot[c], ot[c + 1], ot[c + 2], ot[c + 3]);
+        *reinterpret_cast<float2*>(pl.ws_ml + 2 * slot) = make_float2(m_ref, l);
+      }
+    }
+  } else {
+    // ---------------- gather + dequantise (warps 5..11) ----------------
+    const int g = tid - 32 * (1 + kSoftWarps);  // 0..223
+    constexpr int kTasks = kTok * kChunks;       // 1152 chunks of 16 codes per tile
+    constexpr int kPer = (kTasks + 32 * kGatherWarps - 1) / (32 * kGatherWarps);  // 6
+    for (int j = 0; j < nt; ++j) {
+      const int b = j & 1;
+      uint8_t* kv = s_kv + b * kKvBytes;
+      tc::mbar_wait(&ctl.kv_empty[b], ((j >> 1) & 1) ^ 1, abort, a.status);
+      const int e0 = (tile0 + j) * kTok;
+      uint4 code[kPer];
+      float scl[kPer];
+      bool live[kPer];
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = g + k * 32 * kGatherWarps;
+        live[k] = false;
+        code[k] = make_uint4(0u, 0u, 0u, 0u);
+        scl[k] = 0.f;
+        if (i < kTasks) {
+          const int tok = i / kChunks, c = i % kChunks;
+          const uint8_t* rec = record(e0 + tok, c == 0);
+          if (rec) {
+            live[k] = true;
+            code[k] = __ldg(reinterpret_cast<const uint4*>(rec + 16 * c));
+            scl[k] = __ldg(reinterpret_cast<const float*>(rec + kKvScaleOff) + (c >> 3));
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = g + k * 32 * kGatherWarps;
+        if (i >= kTasks) continue;
+        const int tok = i / kChunks, c = i % kChunks;
+        uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+        if (live[k]) {
+          const uint32_t w[4] = {code[k].x, code[k].y, code[k].z, code[k].w};
+          uint32_t o[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float f[4];
+            e4m3x4_to_f32(w[q], f);
+            o[2 * q] = pack_bf16(f[0] * scl[k], f[1] * scl[k]);
+            o[2 * q + 1] = pack_bf16(f[2] * scl[k], f[3] * scl[k]);
+          }
+          o0 = make_uint4(o[0], o[1], o[2], o[3]);
+          o1 = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        const int kb = c >> 2, cc = (c & 3) * 2;
+        uint8_t* row = kv + kb * kKvBlock + tok * 128;
+        *reinterpret_cast<uint4*>(row + ((cc ^ (tok & 7)) << 4)) = o0;
+        *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (tok & 7)) << 4)) = o1;
+      }
+      tc::fence_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&ctl.kv_full[b]);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+// Merge the splits of each (row, head): weights 2^(m_s - M), M = max_s m_s.
+__global__ void __launch_bounds__(128)
+sfa_combine_kernel(SfaArgs a, SfaPlan pl) {
+  const int t = blockIdx.x, h = blockIdx.y;
+  const int ns = pl.nsplit;
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, pl.ws_ml[2 * ((static_cast<size_t>(t) * ns + s) * a.h_s + h)]);
+  float wsum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < ns; ++s) {
+    const size_t slot = (static_cast<size_t>(t) * ns + s) * a.h_s + h;
+    const float ms = pl.ws_ml[2 * slot], ls = pl.ws_ml[2 * slot + 1];
+    const float wgt = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+    wsum += wgt * ls;
+    const float4 v = *reinterpret_cast<const float4*>(pl.ws_o + slot * kVDim + 4 * threadIdx.x);
+    acc.x += wgt * v.x; acc.y += wgt * v.y; acc.z += wgt * v.z; acc.w += wgt * v.w;
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(t) * a.h_s + h) * kVDim;
+  *reinterpret_cast<uint2*>(out + 4 * threadIdx.x) =
+      make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+  if (a.out_lse && threadIdx.x == 0)
+    a.out_lse[static_cast<size_t>(t) * a.h_s + h] =
+        wsum > 0.f ? (M + log2f(wsum)) * 0.6931471805599453f : -INFINITY;
+}
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
+
+size_t ws_o_bytes(int n_q, int h_s, int ns) {
+  return (static_cast<size_t>(n_q) * ns * h_s * kVDim * sizeof(float) + 255) / 256 * 256;
+}
+
+}  // namespace
+
+size_t sfa_workspace_bytes(int n_q, int h_s, int topk) {
+  const int ns = split_count(n_q, topk);
+  if (ns <= 1) return 0;
+  return ws_o_bytes(n_q, h_s, ns) + static_cast<size_t>(n_q) * ns * h_s * 2 * sizeof(float);
+}
+
+cudaError_t launch_sfa(const SfaArgs& a, cudaStream_t s, const char** err) {
+  if (a.n_q == 0) return cudaSuccess;
+  SfaPlan pl{};
+  pl.nsplit = split_count(a.n_q, a.topk);
+  pl.tiles_total = (a.topk + kTok - 1) / kTok;
+  if (pl.nsplit > 1) {
+    pl.ws_o = static_cast<float*>(a.workspace);
+    pl.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + ws_o_bytes(a.n_q, a.h_s, pl.nsplit));
+  }
+  EncodeFn enc = encode_fn();
+  if (!enc) {
+    *err = "sparse_attn: cuTensorMapEncodeTiled is not available";
+    return cudaErrorNotSupported;
+  }
+  CUtensorMap qmap;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kLatent), static_cast<cuuint64_t>(a.h_s),
+                              static_cast<cuuint64_t>(a.n_q)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kLatent) * 2,
+                                 static_cast<cuuint64_t>(kLatent) * 2 * static_cast<cuuint64_t>(a.h_s)};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+    *err = "sparse_attn: tensor map encoding failed";
+    return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  sfa_tc_kernel<<<dim3(pl.nsplit, a.n_q), kThreads, kSmemBytes, s>>>(qmap, a, pl);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || pl.nsplit == 1) return e;
+  sfa_combine_kernel<<<dim3(a.n_q, a.h_s), 128, 0, s>>>(a, pl);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

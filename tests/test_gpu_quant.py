@@ -93,7 +93,7 @@ def test_cache_writers_special_values_bit_exact(dsa):
 
 
 def test_negative_slots_skip_and_out_of_range_slots_flag(dsa):
-    k = _special_rows(128, 4, 3).cuda()
+    k = _special_rows(128, 64, 3)[:4].contiguous().cuda()
     kc = dsa.alloc_k_cache(1)
     kc.fill_(0xAB)
     dsa.quant_kv_mxfp8(k, torch.tensor([-1, 0, 64, -5], dtype=torch.int64, device="cuda"), kc)
