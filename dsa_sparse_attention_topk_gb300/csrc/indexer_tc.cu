@@ -20,9 +20,10 @@
 //              copies them to TMEM and issues four block-scaled MXFP8 MMAs
 //              (M = 128 positions, N = G * Hp query heads, K = 4 x 32) into a
 //              double-buffered TMEM accumulator;
-//   warps 2-5  epilogue: one TMEM lane (= one position) per thread, ReLU, head weights and
-//              the sum over heads in registers, then the score's order-preserving key goes
-//              to shared memory.  No score leaves the chip.
+//   warps 2-9  epilogue, two sets of four warps (set s drains accumulator s): one TMEM
+//              lane (= one position) per thread, ReLU, head weights and the sum over heads
+//              in registers; the score's order-preserving key goes to shared memory and its
+//              top radix digit into a histogram for the selection.  No score leaves the chip.
 // The MXFP8 queries are quantised on chip into the MMA's B operand at kernel start.  After
 // the scan, the cluster selects the Top-K of every row over distributed shared memory
 // (topk_cluster.cuh).
@@ -39,7 +40,8 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 192;          // 6 warps
+constexpr int kEpiWarps = 8;           // two sets of four epilogue warps (one per accumulator)
+constexpr int kThreads = 32 * (2 + kEpiWarps);  // 10 warps
 constexpr int kTileP = 128;            // positions per MMA tile = two pages
 constexpr int kStageA = kTileP * kIdxDim;        // 16384 B of E4M3 codes
 constexpr int kStageSF = kTileP * 4;             // 512 B of E8M0 scales (position order)
@@ -51,8 +53,11 @@ struct Plan {
   int G, H, Hp, Np, nacc, stages, chunk_cap;
   uint32_t tmem_cols, d_col[2], sfa_col[2], sfb_col;
   // dynamic shared memory offsets (from a 1024-byte aligned base)
-  uint32_t off_stage, off_b, off_sfb, off_w, off_keys, off_topk, off_bar, total;
+  uint32_t off_stage, off_b, off_sfb, off_w, off_keys, off_hist0, off_topk, off_bar, total;
 };
+
+// Query heads padded to the MMA's N granularity: 16, 32 or 64 rows per query row.
+__host__ __device__ constexpr int padded_heads(int h) { return h <= 16 ? 16 : (h <= 32 ? 32 : 64); }
 
 struct Barriers {
   uint64_t full[kMaxStages];
@@ -72,7 +77,7 @@ __host__ inline Plan make_plan(int G, int H, int chunk_cap, int stages) {
   Plan p{};
   p.G = G;
   p.H = H;
-  p.Hp = (H + 15) / 16 * 16;
+  p.Hp = padded_heads(H);
   p.Np = G * p.Hp;
   p.nacc = p.Np <= 128 ? 2 : 1;
   p.stages = stages;
@@ -92,6 +97,7 @@ __host__ inline Plan make_plan(int G, int H, int chunk_cap, int stages) {
   p.off_sfb = o = align_up(o, 16); o += 2 * 512;
   p.off_w = o; o += 4 * G * p.Hp;
   p.off_keys = o = align_up(o, 16); o += 4u * G * chunk_cap;
+  p.off_hist0 = o; o += 4u * G * kHistBins;
   p.off_topk = o = align_up(o, 16); o += sizeof(TopkSmem);
   p.off_bar = o = align_up(o, 16); o += sizeof(Barriers);
   p.total = o;
@@ -121,7 +127,7 @@ __device__ __forceinline__ uint32_t quant_row_to_b(const __nv_bfloat16* src, uin
   return static_cast<uint32_t>(e + 127);
 }
 
-template <int G>
+template <int G, int HP>
 __global__ void __launch_bounds__(kThreads, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan pl) {
   extern __shared__ uint8_t smem_dyn[];
@@ -132,15 +138,18 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
   uint32_t* s_sfb = reinterpret_cast<uint32_t*>(smem + pl.off_sfb);
   float* s_w = reinterpret_cast<float*>(smem + pl.off_w);
   uint32_t* s_keys = reinterpret_cast<uint32_t*>(smem + pl.off_keys);
+  uint32_t* s_hist0 = reinterpret_cast<uint32_t*>(smem + pl.off_hist0);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = static_cast<int>(cluster_ctarank());
   const int C = static_cast<int>(cluster_nctarank());
   const int row0 = blockIdx.y * G;
-  const int H = pl.H, Hp = pl.Hp, Np = pl.Np, S = pl.stages;
+  const int H = pl.H, S = pl.stages;
+  constexpr int Hp = HP, Np = G * HP;
 
   // ---- prologue -------------------------------------------------------------------
   topk_init(tk);
+  for (int i = tid; i < G * kHistBins; i += kThreads) s_hist0[i] = 0;
   if (tid == 0) {
     int seq = a.q_seq[row0];
     unsigned bad = 0;
@@ -285,10 +294,11 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
       __syncwarp();
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (warps 2..9) ----------------
+    const int set = (warp - 2) >> 2;           // which accumulator this warp drains
     const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
     const int m = quarter * 32 + lane;         // tile row = position offset in the tile
-    for (int t = 0; t < ntiles; ++t) {
+    for (int t = set; t < (set < pl.nacc ? ntiles : 0); t += pl.nacc) {
       const int acc = t % pl.nacc, ia = t / pl.nacc;
       const bool ok = tc::mbar_wait(&bs.tfull[acc], ia & 1, abort, a.status);
       tc::fence_after_sync();
@@ -298,15 +308,15 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
       float sc[G];
 #pragma unroll
       for (int j = 0; j < G; ++j) {
-        float s = 0.f;
-        for (int h0 = 0; h0 < Hp; h0 += 16) {
-          uint32_t r[16];
-          tc::tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + pl.d_col[acc] + j * Hp + h0, r);
-          tc::tmem_wait_ld();
-          const float* wj = s_w + j * Hp + h0;
+        uint32_t r[HP];
+        const uint32_t col = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + pl.d_col[acc] + j * HP;
 #pragma unroll
-          for (int h = 0; h < 16; ++h) s = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.f), s);
-        }
+        for (int h0 = 0; h0 < HP; h0 += 16) tc::tmem_ld16(col + h0, reinterpret_cast<uint32_t(&)[16]>(r[h0]));
+        tc::tmem_wait_ld();
+        const float* wj = s_w + j * HP;
+        float s = 0.f;
+#pragma unroll
+        for (int h = 0; h < HP; ++h) s = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.f), s);
         sc[j] = s;
       }
       tc::fence_before_sync();
@@ -314,7 +324,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
 #pragma unroll
       for (int j = 0; j < G; ++j) {
         const bool valid = ok && page_ok && local < len && p < bs.n_sel[j];
-        s_keys[j * pl.chunk_cap + local] = valid ? score_key(sc[j]) : 0u;
+        const uint32_t key = valid ? score_key(sc[j]) : 0u;
+        s_keys[j * pl.chunk_cap + local] = key;
+        hist_add_top_digit(s_hist0 + j * kHistBins, key);
         if (a.out_full && valid) a.out_full[static_cast<size_t>(row0 + j) * a.max_ctx + p] = sc[j];
       }
     }
@@ -326,8 +338,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
 #pragma unroll 1
     for (int j = 0; j < G; ++j) {
       const size_t row = static_cast<size_t>(row0 + j);
-      cluster_topk_row(tk, s_keys + j * pl.chunk_cap, c0, len, bs.n_sel[j], a.topk, a.out_idx + row * a.topk,
-                       a.out_scores ? a.out_scores + row * a.topk : nullptr);
+      cluster_topk_row(tk, s_keys + j * pl.chunk_cap, s_hist0 + j * kHistBins, c0, len, bs.n_sel[j], a.topk,
+                       a.out_idx + row * a.topk, a.out_scores ? a.out_scores + row * a.topk : nullptr);
     }
   }
   cluster_sync();  // no CTA leaves while its shared memory may still be addressed
@@ -372,8 +384,8 @@ DevInfo dev_info() {
   return d;
 }
 
-template <int G>
-cudaError_t launch_g(const IndexerArgs& a, cudaStream_t s, const char** err) {
+template <int G, int HP>
+cudaError_t launch_gh(const IndexerArgs& a, cudaStream_t s, const char** err) {
   const DevInfo di = dev_info();
   const int n_groups = a.n_q / G;
   const size_t limit = static_cast<size_t>(di.smem_optin) - 1024;  // room for the 1024-byte alignment
@@ -413,7 +425,7 @@ cudaError_t launch_g(const IndexerArgs& a, cudaStream_t s, const char** err) {
     *err = "indexer: tensor map encoding failed";
     return cudaErrorInvalidValue;
   }
-  auto kern = indexer_tc_kernel<G>;
+  auto kern = indexer_tc_kernel<G, HP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (C > 8) {
@@ -437,6 +449,15 @@ cudaError_t launch_g(const IndexerArgs& a, cudaStream_t s, const char** err) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, map, a, pl);
+}
+
+template <int G>
+cudaError_t launch_g(const IndexerArgs& a, cudaStream_t s, const char** err) {
+  switch (padded_heads(a.h_i)) {
+    case 16: return launch_gh<G, 16>(a, s, err);
+    case 32: return launch_gh<G, 32>(a, s, err);
+    default: return launch_gh<G, 64>(a, s, err);
+  }
 }
 
 }  // namespace

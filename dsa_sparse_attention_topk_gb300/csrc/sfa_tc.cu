@@ -67,13 +67,15 @@ struct Ctl {
   uint64_t s_free;
   uint32_t tmem_base;
   int abort;
+  uint8_t valid[2][kTok];  // per KV buffer: selected entry t of the tile is a real cache row
 };
 
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKv = kQBytes;
 constexpr uint32_t kOffP = kOffKv + 2 * kKvBytes;
 constexpr uint32_t kOffCtl = kOffP + kPBytes;
-constexpr uint32_t kSmemBytes = kOffCtl + 128 + 1024;  // + slack for the 1024-byte alignment
+constexpr uint32_t kCtlBytes = 256;
+constexpr uint32_t kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + slack for the 1024-byte alignment
 
 __host__ __device__ inline int split_count(int n_q, int topk) {
   const int tiles = (topk + kTok - 1) / kTok;
@@ -86,7 +88,7 @@ __host__ __device__ inline int split_count(int n_q, int topk) {
 struct SfaPlan {
   int nsplit, tiles_total;
   float* ws_o;    // [n_q][nsplit][h_s][512] unnormalised partial outputs
-  float* ws_ml;   // [n_q][nsplit][h_s][2] running max (log2 domain) and sum
+  float* ws_ml;   // [n_q][nsplit][h_s][4] running max (log2 domain), rounded and exact sums
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -199,13 +201,16 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     const int m = quarter * 32 + lane;  // head row
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const float c2 = a.sm_scale * 1.4426950408889634f;  // logits in log2 units
-    float m_ref = -INFINITY, l = 0.f;
+    // l sums the bf16-rounded weights that the P V product uses (it normalises O);
+    // lx sums the unrounded weights (it gives the log-sum-exp)
+    float m_ref = -INFINITY, l = 0.f, lx = 0.f;
     float ot[kVTail];
 #pragma unroll
     for (int i = 0; i < kVTail; ++i) ot[i] = 0.f;
     for (int j = 0; j < nt; ++j) {
-      const int e = (tile0 + j) * kTok + lane;
-      const uint32_t mask = __ballot_sync(0xffffffffu, record(e, false) != nullptr);
+      // the gather warps flag the tile's real entries before they release the buffer
+      tc::mbar_wait(&ctl.kv_full[j & 1], (j >> 1) & 1, abort, a.status);
+      const uint32_t mask = __ballot_sync(0xffffffffu, ctl.valid[j & 1][lane] != 0);
       tc::mbar_wait(&ctl.s_full, j & 1, abort, a.status);
       tc::fence_after_sync();
       uint32_t sr[32];
@@ -236,18 +241,21 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
 #pragma unroll
       for (int i = 0; i < kVTail; ++i) ot[i] *= alpha;
       l *= alpha;
+      lx *= alpha;
       m_ref = m_new;
       uint32_t pk[16];
-      float lsum = 0.f;
+      float lsum = 0.f, lxsum = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; i += 2) {
         const float p0 = (m_ref == -INFINITY) ? 0.f : exp2f(x[i] - m_ref);
         const float p1 = (m_ref == -INFINITY) ? 0.f : exp2f(x[i + 1] - m_ref);
         const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
         lsum += __low2float(pb) + __high2float(pb);
+        lxsum += p0 + p1;
         pk[i >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
       }
       l += lsum;
+      lx += lxsum;
       // P row m: core matrix (m/8, chunk c) at (m/8)*512 + c*128, row offset (m%8)*16
       uint8_t* prow = s_p + (m >> 3) * 512 + (m & 7) * 16;
 #pragma unroll
@@ -306,7 +314,7 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
                          pack_bf16(ot[c + 4] * inv, ot[c + 5] * inv), pack_bf16(ot[c + 6] * inv, ot[c + 7] * inv));
         }
         if (a.out_lse)
-          a.out_lse[static_cast<size_t>(t) * a.h_s + m] = l > 0.f ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
+          a.out_lse[static_cast<size_t>(t) * a.h_s + m] = lx > 0.f ? (m_ref + log2f(lx)) * 0.6931471805599453f : -INFINITY;
       }
     } else {
       const size_t slot = (static_cast<size_t>(t) * pl.nsplit + split) * a.h_s + m;
@@ -330,7 +338,7 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
 #pragma unroll
         for (int c = 0; c < kVTail; c += 4)
           *reinterpret_cast<float4*>(wo + kVLeft + c) = make_float4(ot[c], ot[c + 1], ot[c + 2], ot[c + 3]);
-        *reinterpret_cast<float2*>(pl.ws_ml + 2 * slot) = make_float2(m_ref, l);
+        *reinterpret_cast<float4*>(pl.ws_ml + 4 * slot) = make_float4(m_ref, l, lx, 0.f);
       }
     }
   } else {
@@ -338,14 +346,22 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     const int g = tid - 32 * (1 + kSoftWarps);  // 0..223
     constexpr int kTasks = kTok * kChunks;       // 1152 chunks of 16 codes per tile
     constexpr int kPer = (kTasks + 32 * kGatherWarps - 1) / (32 * kGatherWarps);  // 6
-    for (int j = 0; j < nt; ++j) {
-      const int b = j & 1;
-      uint8_t* kv = s_kv + b * kKvBytes;
-      tc::mbar_wait(&ctl.kv_empty[b], ((j >> 1) & 1) ^ 1, abort, a.status);
-      const int e0 = (tile0 + j) * kTok;
-      uint4 code[kPer];
-      float scl[kPer];
-      bool live[kPer];
+    // Warm L1 with this split's index list and the sequence's page-table row, so that the
+    // index -> page -> record lookups below are cache hits.
+    {
+      const int e_lo = tile0 * kTok, e_hi = min(a.topk, (tile0 + nt) * kTok);
+      for (int e = e_lo + g * 32; e < e_hi; e += 32 * 32 * kGatherWarps)
+        asm volatile("prefetch.global.L1 [%0];" :: "l"(idx + e));
+      const int npg = min(a.max_pages, (L + kPage - 1) / kPage);
+      for (int pg = g * 32; pg < npg; pg += 32 * 32 * kGatherWarps)
+        asm volatile("prefetch.global.L1 [%0];" :: "l"(ptab + pg));
+    }
+    uint4 code[kPer];
+    float scl[kPer];
+    bool live[kPer];
+    // load the codes of tile jj into the registers (one tile ahead of the conversion)
+    auto load_tile = [&](int jj) {
+      const int e0 = (tile0 + jj) * kTok;
 #pragma unroll
       for (int k = 0; k < kPer; ++k) {
         const int i = g + k * 32 * kGatherWarps;
@@ -357,17 +373,25 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
           const uint8_t* rec = record(e0 + tok, c == 0);
           if (rec) {
             live[k] = true;
-            code[k] = __ldg(reinterpret_cast<const uint4*>(rec + 16 * c));
-            scl[k] = __ldg(reinterpret_cast<const float*>(rec + kKvScaleOff) + (c >> 3));
+            asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(code[k].x), "=r"(code[k].y), "=r"(code[k].z), "=r"(code[k].w)
+                         : "l"(rec + 16 * c));
+            asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];"
+                         : "=f"(scl[k]) : "l"(rec + kKvScaleOff + 4 * (c >> 3)));
           }
         }
       }
+    };
+    if (nt > 0) load_tile(0);
+    for (int j = 0; j < nt; ++j) {
+      const int b = j & 1;
+      uint8_t* kv = s_kv + b * kKvBytes;
+      tc::mbar_wait(&ctl.kv_empty[b], ((j >> 1) & 1) ^ 1, abort, a.status);
+      uint4 o0s[kPer], o1s[kPer];
 #pragma unroll
       for (int k = 0; k < kPer; ++k) {
-        const int i = g + k * 32 * kGatherWarps;
-        if (i >= kTasks) continue;
-        const int tok = i / kChunks, c = i % kChunks;
-        uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+        o0s[k] = make_uint4(0u, 0u, 0u, 0u);
+        o1s[k] = o0s[k];
         if (live[k]) {
           const uint32_t w[4] = {code[k].x, code[k].y, code[k].z, code[k].w};
           uint32_t o[8];
@@ -378,13 +402,24 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
             o[2 * q] = pack_bf16(f[0] * scl[k], f[1] * scl[k]);
             o[2 * q + 1] = pack_bf16(f[2] * scl[k], f[3] * scl[k]);
           }
-          o0 = make_uint4(o[0], o[1], o[2], o[3]);
-          o1 = make_uint4(o[4], o[5], o[6], o[7]);
+          o0s[k] = make_uint4(o[0], o[1], o[2], o[3]);
+          o1s[k] = make_uint4(o[4], o[5], o[6], o[7]);
         }
+      }
+      bool flag_live[kPer];
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) flag_live[k] = live[k];
+      if (j + 1 < nt) load_tile(j + 1);  // next tile's loads fly while this one is stored
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = g + k * 32 * kGatherWarps;
+        if (i >= kTasks) continue;
+        const int tok = i / kChunks, c = i % kChunks;
         const int kb = c >> 2, cc = (c & 3) * 2;
         uint8_t* row = kv + kb * kKvBlock + tok * 128;
-        *reinterpret_cast<uint4*>(row + ((cc ^ (tok & 7)) << 4)) = o0;
-        *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (tok & 7)) << 4)) = o1;
+        *reinterpret_cast<uint4*>(row + ((cc ^ (tok & 7)) << 4)) = o0s[k];
+        *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (tok & 7)) << 4)) = o1s[k];
+        if (c == 0) ctl.valid[b][tok] = flag_live[k] ? 1 : 0;
       }
       tc::fence_async_smem();
       __syncwarp();
@@ -403,14 +438,15 @@ sfa_combine_kernel(SfaArgs a, SfaPlan pl) {
   const int t = blockIdx.x, h = blockIdx.y;
   const int ns = pl.nsplit;
   float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, pl.ws_ml[2 * ((static_cast<size_t>(t) * ns + s) * a.h_s + h)]);
-  float wsum = 0.f;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, pl.ws_ml[4 * ((static_cast<size_t>(t) * ns + s) * a.h_s + h)]);
+  float wsum = 0.f, wsum_x = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s = 0; s < ns; ++s) {
     const size_t slot = (static_cast<size_t>(t) * ns + s) * a.h_s + h;
-    const float ms = pl.ws_ml[2 * slot], ls = pl.ws_ml[2 * slot + 1];
-    const float wgt = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-    wsum += wgt * ls;
+    const float4 ml = *reinterpret_cast<const float4*>(pl.ws_ml + 4 * slot);
+    const float wgt = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+    wsum += wgt * ml.y;
+    wsum_x += wgt * ml.z;
     const float4 v = *reinterpret_cast<const float4*>(pl.ws_o + slot * kVDim + 4 * threadIdx.x);
     acc.x += wgt * v.x; acc.y += wgt * v.y; acc.z += wgt * v.z; acc.w += wgt * v.w;
   }
@@ -420,7 +456,7 @@ sfa_combine_kernel(SfaArgs a, SfaPlan pl) {
       make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
   if (a.out_lse && threadIdx.x == 0)
     a.out_lse[static_cast<size_t>(t) * a.h_s + h] =
-        wsum > 0.f ? (M + log2f(wsum)) * 0.6931471805599453f : -INFINITY;
+        wsum_x > 0.f ? (M + log2f(wsum_x)) * 0.6931471805599453f : -INFINITY;
 }
 
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -448,7 +484,7 @@ size_t ws_o_bytes(int n_q, int h_s, int ns) {
 size_t sfa_workspace_bytes(int n_q, int h_s, int topk) {
   const int ns = split_count(n_q, topk);
   if (ns <= 1) return 0;
-  return ws_o_bytes(n_q, h_s, ns) + static_cast<size_t>(n_q) * ns * h_s * 2 * sizeof(float);
+  return ws_o_bytes(n_q, h_s, ns) + static_cast<size_t>(n_q) * ns * h_s * 4 * sizeof(float);
 }
 
 cudaError_t launch_sfa(const SfaArgs& a, cudaStream_t s, const char** err) {

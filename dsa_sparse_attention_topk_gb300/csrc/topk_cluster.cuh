@@ -5,9 +5,12 @@
 // write-back.  Each CTA of the cluster holds the order-preserving keys of one contiguous
 // chunk of positions in shared memory (key 0 = not selectable).  The K-th largest key T
 // is found by a three-digit radix select (11 + 11 + 10 bits) whose histograms are summed
-// in the leader CTA's shared memory through distributed shared memory; then every CTA
-// writes its positions with key > T, and the lowest positions with key == T up to K
-// (CTA rank order is position order, so the tie quota is handed out rank by rank).
+// in the leader CTA's shared memory through distributed shared memory.  The first
+// digit's local histogram is built while the scores are produced; the later digits only
+// touch keys that share the selected prefix.  Every CTA then writes its positions with
+// key > T, and the lowest positions with key == T up to K (CTA rank order is position
+// order, so the tie quota is handed out rank by rank).  The output of every CTA is in
+// position order, so the result is deterministic.
 #pragma once
 
 #include "dsa_common.cuh"
@@ -20,10 +23,10 @@ constexpr int kHistBins = 2048;
 // cluster-wide one).
 struct TopkSmem {
   uint32_t hist[2][kHistBins];   // leader: cluster histograms (double-buffered)
-  uint32_t local[kHistBins];     // every CTA: its own histogram
+  uint32_t local[kHistBins];     // every CTA: its histogram of the current digit
   uint32_t counts[2][16];        // leader: per-rank (count_gt, count_eq)
   uint32_t bcast[2];             // every CTA: (digit, count_above) sent by the leader
-  uint32_t warp_tot[2][32];      // block scan scratch
+  uint32_t warp_cnt[2][32];      // per-warp counts for the ordered compaction
 };
 
 // Zero the leader's histograms; call before the first cluster_sync of the kernel.
@@ -31,37 +34,62 @@ __device__ __forceinline__ void topk_init(TopkSmem& sm) {
   for (int i = threadIdx.x; i < 2 * kHistBins; i += blockDim.x) (&sm.hist[0][0])[i] = 0;
 }
 
-// Block-wide exclusive scan of two 0/1 flags; returns the exclusive prefix of each and
-// writes the block totals.
-__device__ __forceinline__ void block_scan2(TopkSmem& sm, uint32_t f0, uint32_t f1, uint32_t& p0,
-                                            uint32_t& p1, uint32_t& t0, uint32_t& t1) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const uint32_t b0 = __ballot_sync(0xffffffffu, f0), b1 = __ballot_sync(0xffffffffu, f1);
-  const uint32_t lt = (1u << lane) - 1u;
-  if (lane == 0) { sm.warp_tot[0][warp] = __popc(b0); sm.warp_tot[1][warp] = __popc(b1); }
-  __syncthreads();
-  uint32_t o0 = 0, o1 = 0, s0 = 0, s1 = 0;
-  for (int i = 0; i < nw; ++i) {
-    const uint32_t a = sm.warp_tot[0][i], b = sm.warp_tot[1][i];
-    if (i < warp) { o0 += a; o1 += b; }
-    s0 += a; s1 += b;
+// Add `key`'s top digit (bits 31..21) to a local histogram, aggregated over the warp.
+// Every lane of the warp must call it (key 0 = nothing to add).
+__device__ __forceinline__ void hist_add_top_digit(uint32_t* hist, uint32_t key) {
+  const uint32_t d = key ? (key >> 21) : 0xFFFFFFFFu;
+  const uint32_t peers = __match_any_sync(0xffffffffu, d);
+  if (key && (__ffs(peers) - 1) == static_cast<int>(threadIdx.x & 31)) atomicAdd(&hist[d], __popc(peers));
+}
+
+// Leader: find the digit (scanning down from the top bin) where the running count of
+// cl_hist reaches `need`, send (digit, count above it) to every rank, zero cl_hist.
+__device__ __forceinline__ void leader_pick(TopkSmem& sm, uint32_t* cl_hist, uint32_t need, uint32_t nrank) {
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    const int per = kHistBins / 32;
+    const int lane = tid;
+    const int hi = kHistBins - lane * per;  // lane 0 owns the top slice [hi - per, hi)
+    uint32_t slice = 0;
+    for (int j = hi - per; j < hi; ++j) slice += cl_hist[j];
+    uint32_t incl = slice;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const uint32_t excl = incl - slice;
+    const uint32_t who = __ballot_sync(0xffffffffu, (excl < need) && (need <= incl));
+    if (lane == __ffs(who) - 1) {
+      uint32_t run = excl, found_d = 0, found_above = 0;
+      bool found = false;
+      for (int j = hi - 1; j >= hi - per; --j) {
+        const uint32_t c = cl_hist[j];
+        if (!found && run + c >= need) { found = true; found_d = j; found_above = run; }
+        run += c;
+      }
+      for (uint32_t r = 0; r < nrank; ++r) {
+        dsmem_st_u32(dsmem_addr(&sm.bcast[0], r), found_d);
+        dsmem_st_u32(dsmem_addr(&sm.bcast[1], r), found_above);
+      }
+    }
   }
-  p0 = o0 + __popc(b0 & lt);
-  p1 = o1 + __popc(b1 & lt);
-  t0 = s0; t1 = s1;
   __syncthreads();
+  for (int i = tid; i < kHistBins; i += blockDim.x) cl_hist[i] = 0;  // ready for reuse
 }
 
 // Select the Top-K of one query row.
 //   keys[0..len)  this CTA's keys for positions c0 .. c0+len-1 (0 = not selectable)
+//   hist0         this CTA's histogram of the keys' top digit (bits 31..21); it is
+//                 consumed (left in an unspecified state)
 //   n_sel         number of selectable positions of the row (positions 0..n_sel-1)
 // Writes out_idx[0..K) (and out_scores if non-null).  Must be called by every thread of
 // every CTA of the cluster (it contains cluster barriers).
-__device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, int c0, int len, int n_sel,
+__device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, uint32_t* hist0, int c0, int len, int n_sel,
                                  int K, int32_t* out_idx, float* out_scores) {
   const uint32_t rank = cluster_ctarank();
   const uint32_t nrank = cluster_nctarank();
-  const int tid = threadIdx.x, nt = blockDim.x;
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
 
   if (n_sel <= K) {
     // every selectable position is kept, in position order; rank 0 pads the tail
@@ -83,94 +111,48 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, int c0, int
 
   uint32_t prefix = 0;
   uint32_t need = static_cast<uint32_t>(K);
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
+  uint32_t my_gt = 0;   // this CTA's keys above the prefix chosen so far (thread 0's copy)
+  uint32_t my_eq = 0;
 #pragma unroll 1
   for (int lvl = 0; lvl < 3; ++lvl) {
-    const int sh = shifts[lvl];
-    const uint32_t mask = (1u << widths[lvl]) - 1u;
-    const int hsh = sh + widths[lvl];  // bits above this digit must equal prefix's
+    const int sh = lvl == 0 ? 21 : (lvl == 1 ? 10 : 0);
+    const int width = lvl == 2 ? 10 : 11;
+    const uint32_t mask = (1u << width) - 1u;
+    const int hsh = sh + width;  // bits above this digit must equal prefix's
+    uint32_t* lh = lvl == 0 ? hist0 : sm.local;
     uint32_t* cl_hist = sm.hist[lvl & 1];
-    for (int i = tid; i < kHistBins; i += nt) sm.local[i] = 0;
-    __syncthreads();
-    for (int base = 0; base < len; base += nt) {  // uniform trip count: whole warps
-      const int i = base + tid;
-      const uint32_t k = (i < len) ? keys[i] : 0u;
-      const bool hit = (k != 0u) && (hsh >= 32 || (k >> hsh) == (prefix >> hsh));
-      const uint32_t d = hit ? ((k >> sh) & mask) : 0xFFFFFFFFu;
-      // warp-aggregated shared atomics: scores crowd into a few top-digit bins
-      const uint32_t peers = __match_any_sync(0xffffffffu, d);
-      if (hit && (__ffs(peers) - 1) == (tid & 31)) atomicAdd(&sm.local[d], __popc(peers));
+    if (lvl > 0) {
+      __syncthreads();  // thread 0 has finished reading the previous digit's histogram
+      for (int i = tid; i < kHistBins; i += nt) sm.local[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < len; i += nt) {
+        const uint32_t k = keys[i];
+        if (k != 0u && (k >> hsh) == (prefix >> hsh)) atomicAdd(&sm.local[(k >> sh) & mask], 1u);
+      }
     }
     __syncthreads();
     for (int i = tid; i < kHistBins; i += nt) {
-      const uint32_t c = sm.local[i];
+      const uint32_t c = lh[i];
       if (c) dsmem_add_u32(dsmem_addr(&cl_hist[i], 0), c);
     }
     cluster_sync();
-    if (rank == 0) {
-      // find digit d (scanning from the top) where the running count reaches `need`
-      if (tid < 32) {
-        uint32_t run = 0, found_d = 0, found_above = 0;
-        bool found = false;
-        const int per = kHistBins / 32;  // each lane sums one 64-bin slice (top slice first)
-        const int lane = tid;
-        const int hi = kHistBins - lane * per;  // slice [hi - per, hi)
-        uint32_t slice = 0;
-        for (int j = hi - per; j < hi; ++j) slice += cl_hist[j];
-        // inclusive prefix over lanes (lane 0 = top slice)
-        uint32_t incl = slice;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        const uint32_t excl = incl - slice;
-        const bool mine = (excl < need) && (need <= incl);
-        const uint32_t who = __ballot_sync(0xffffffffu, mine);
-        const int src = __ffs(who) - 1;
-        if (lane == src) {
-          run = excl;
-          for (int j = hi - 1; j >= hi - per; --j) {
-            const uint32_t c = cl_hist[j];
-            if (!found && run + c >= need) { found = true; found_d = j; found_above = run; }
-            run += c;
-          }
-          for (uint32_t r = 0; r < nrank; ++r) {
-            dsmem_st_u32(dsmem_addr(&sm.bcast[0], r), found_d);
-            dsmem_st_u32(dsmem_addr(&sm.bcast[1], r), found_above);
-          }
-        }
-      }
-      __syncthreads();
-      for (int i = tid; i < kHistBins; i += nt) cl_hist[i] = 0;  // ready for reuse
-    }
+    if (rank == 0) leader_pick(sm, cl_hist, need, nrank);
     cluster_sync();
-    prefix |= sm.bcast[0] << sh;
+    const uint32_t d = sm.bcast[0];
+    prefix |= d << sh;
     need -= sm.bcast[1];
+    // this CTA's keys in digits above d (all of them are selected)
+    if (tid == 0) {
+      for (uint32_t b = d + 1; b <= mask; ++b) my_gt += lh[b];
+      if (lvl == 2) my_eq = lh[d];
+    }
   }
   const uint32_t T = prefix;
   const uint32_t need_eq = need;  // >= 1
 
-  // count > T and == T locally, publish to the leader
-  uint32_t n_gt = 0, n_eq = 0;
-  for (int i = tid; i < len; i += nt) {
-    const uint32_t k = keys[i];
-    n_gt += (k > T);
-    n_eq += (k == T);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    n_gt += __shfl_xor_sync(0xffffffffu, n_gt, o);
-    n_eq += __shfl_xor_sync(0xffffffffu, n_eq, o);
-  }
-  if ((tid & 31) == 0) { sm.warp_tot[0][tid >> 5] = n_gt; sm.warp_tot[1][tid >> 5] = n_eq; }
-  __syncthreads();
   if (tid == 0) {
-    uint32_t a = 0, b = 0;
-    for (int i = 0; i < (nt >> 5); ++i) { a += sm.warp_tot[0][i]; b += sm.warp_tot[1][i]; }
-    dsmem_st_u32(dsmem_addr(&sm.counts[0][rank], 0), a);
-    dsmem_st_u32(dsmem_addr(&sm.counts[1][rank], 0), b);
+    dsmem_st_u32(dsmem_addr(&sm.counts[0][rank], 0), my_gt);
+    dsmem_st_u32(dsmem_addr(&sm.counts[1][rank], 0), my_eq);
   }
   cluster_sync();
   uint32_t gt_before = 0, eq_before = 0, gt_total = 0;
@@ -180,31 +162,48 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, int c0, int
     if (r < rank) { gt_before += a; eq_before += b; }
     gt_total += a;
   }
-  const uint32_t eq_take_lo = eq_before < need_eq ? eq_before : need_eq;  // first eq slot
-  uint32_t gt_off = gt_before;
-  uint32_t eq_off = gt_total + eq_take_lo;
-  uint32_t eq_left = need_eq - eq_take_lo;  // tie quota still open for this rank onwards
+  const uint32_t eq_lo = eq_before < need_eq ? eq_before : need_eq;
+  const uint32_t eq_quota = need_eq - eq_lo;  // ties this CTA may still take
 
-  // ordered compaction over the chunk (ties must go to the lowest positions)
-  for (int base = 0; base < len; base += nt) {
-    const int i = base + tid;
-    const uint32_t k = (i < len) ? keys[i] : 0u;
-    const uint32_t fg = (k > T), fe = (k == T) && (k != 0u);
-    uint32_t pg, pe, tg, te;
-    block_scan2(sm, fg, fe, pg, pe, tg, te);
-    // (the slot bounds only guard the row against an inconsistent count; they never bind)
-    if (fg && gt_off + pg < static_cast<uint32_t>(K)) {
-      out_idx[gt_off + pg] = c0 + i;
-      if (out_scores) out_scores[gt_off + pg] = key_score(k);
+  // ordered compaction: warp w owns the contiguous slice [w*span, (w+1)*span)
+  const int span = ((len + nw - 1) / nw + 31) / 32 * 32;
+  const int lo = warp * span, hi = min(len, lo + span);
+  uint32_t cg = 0, ce = 0;
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    const uint32_t k = i < hi ? keys[i] : 0u;
+    cg += __popc(__ballot_sync(0xffffffffu, k > T));
+    ce += __popc(__ballot_sync(0xffffffffu, k == T && k != 0u));
+  }
+  if (lane == 0) { sm.warp_cnt[0][warp] = cg; sm.warp_cnt[1][warp] = ce; }
+  __syncthreads();
+  uint32_t og = gt_before, oe = 0;
+  for (int w = 0; w < warp; ++w) { og += sm.warp_cnt[0][w]; oe += sm.warp_cnt[1][w]; }
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    const uint32_t k = i < hi ? keys[i] : 0u;
+    const uint32_t bg = __ballot_sync(0xffffffffu, k > T);
+    const uint32_t be = __ballot_sync(0xffffffffu, k == T && k != 0u);
+    if (k > T) {
+      const uint32_t slot = og + __popc(bg & lt);
+      if (slot < static_cast<uint32_t>(K)) {  // guards the row against an inconsistent count
+        out_idx[slot] = c0 + i;
+        if (out_scores) out_scores[slot] = key_score(k);
+      }
     }
-    if (fe && pe < eq_left && eq_off + pe < static_cast<uint32_t>(K)) {
-      out_idx[eq_off + pe] = c0 + i;
-      if (out_scores) out_scores[eq_off + pe] = key_score(k);
+    if (k == T && k != 0u) {
+      const uint32_t r = oe + __popc(be & lt);
+      if (r < eq_quota) {
+        const uint32_t slot = gt_total + eq_lo + r;
+        if (slot < static_cast<uint32_t>(K)) {
+          out_idx[slot] = c0 + i;
+          if (out_scores) out_scores[slot] = key_score(k);
+        }
+      }
     }
-    gt_off += tg;
-    const uint32_t used = te < eq_left ? te : eq_left;
-    eq_off += used;
-    eq_left -= used;
+    og += __popc(bg);
+    oe += __popc(be);
   }
   // keep the leader's counts alive until every rank has read them
   cluster_sync();

@@ -182,6 +182,18 @@ def check_topk(gpu_idx, gpu_vals, ref_s, mag, k):
     return len(diff)
 
 
+def lse_bound(q_row, kv_hat, idx, sm_scale):
+    """Per-head bound on |lse_gpu - lse_ref|.  The tensor-core path rounds each
+    dequantised latent value to bf16 (relative error <= 2^-9), so every logit moves by at
+    most sm_scale * sum_d |q_d kv_d| * 2^-9, and the log-sum-exp (a weighted mean of the
+    logits' moves) by at most the largest of those; fp32 summation adds a little."""
+    sel = np.asarray(idx)[np.asarray(idx) >= 0]
+    if sel.size == 0:
+        return np.zeros(q_row.shape[0])
+    mag = np.abs(q_row) @ np.abs(kv_hat[sel]).T          # (H, J)
+    return sm_scale * mag.max(axis=1) * 2.0 ** -9 + 1e-4
+
+
 def check_sfa(gpu_o, ref_o):
     g = np.asarray(gpu_o, np.float64)
     d = np.abs(g - ref_o)
