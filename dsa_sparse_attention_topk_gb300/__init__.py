@@ -61,6 +61,8 @@ _SIGS = {
     "dsa_sparse_attn_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "dsa_sparse_attn": (ctypes.c_int, [_P, _I32, _I32, _P, _I64, _P, _I32, _P, _P, _I32, _P, _I32,
                                        _F32, _P, _P, _P, _SZ, _P]),
+    "dsa_sparse_attn_noalloc": (ctypes.c_int, [_P, _I32, _I32, _P, _I64, _P, _I32, _P, _P, _I32, _P, _I32,
+                                               _F32, _P, _P, _P]),
     "dsa_device_status": (ctypes.c_int, [_P]),
     "dsa_last_error": (ctypes.c_char_p, []),
     "dsa_version": (ctypes.c_int, []),
@@ -185,6 +187,26 @@ def sparse_attn(q, kv_cache, page_table, seq_lens, q_seq, topk_idx, sm_scale, ou
                                  _ptr(workspace), 0 if workspace is None else workspace.numel(),
                                  _stream(stream)))
     return out, out_lse
+
+
+def sparse_attn_noalloc(q, kv_cache, page_table, seq_lens, q_seq, topk_idx, sm_scale, out=None,
+                        out_lse=None, stream=None):
+    """Sparse Flash Attention with the split-merge scratch kept in the library's fixed
+    array, for callers that cannot allocate device memory.  Same result as sparse_attn.
+    Calls that overlap on the GPU share that array and must not run concurrently."""
+    n_q, h_s, _ = q.shape
+    topk = topk_idx.shape[1]
+    if out is None:
+        out = torch.empty(n_q, h_s, V_DIM, dtype=torch.bfloat16, device=q.device)
+    num_pages = kv_cache.numel() // (PAGE_SIZE * KVCACHE_TOKEN_BYTES)
+    _check(lib().dsa_sparse_attn_noalloc(_ptr(q), n_q, h_s, _ptr(kv_cache), num_pages, _ptr(page_table),
+                                         page_table.shape[1], _ptr(seq_lens), _ptr(q_seq), seq_lens.shape[0],
+                                         _ptr(topk_idx), topk, float(sm_scale), _ptr(out), _ptr(out_lse),
+                                         _stream(stream)))
+    return out, out_lse
+
+
+NOALLOC_SCRATCH_BYTES = 40 * 1024 * 1024
 
 
 def device_status(stream=None):

@@ -184,6 +184,40 @@ int dsa_sparse_attn(const void* q_bf16, int32_t n_q, int32_t h_s, const uint8_t*
   return DSA_OK;
 }
 
+int dsa_sparse_attn_noalloc(const void* q_bf16, int32_t n_q, int32_t h_s, const uint8_t* kv_cache,
+                            int64_t num_pages, const int32_t* page_table, int32_t max_pages,
+                            const int32_t* seq_lens, const int32_t* q_seq, int32_t n_seq,
+                            const int32_t* topk_idx, int32_t topk, float sm_scale, void* out_bf16,
+                            float* out_lse, void* stream) {
+  if (n_q < 0 || n_seq < 0) return fail(DSA_ERR_INVALID_ARG, "sparse_attn_noalloc: negative n_q or n_seq");
+  if (h_s < 1 || h_s > 128) return fail(DSA_ERR_UNSUPPORTED, "sparse_attn_noalloc: h_s must be 1..128");
+  if (topk < 1 || topk > 65536) return fail(DSA_ERR_UNSUPPORTED, "sparse_attn_noalloc: topk must be 1..65536");
+  if (max_pages < 1 || num_pages < 1)
+    return fail(DSA_ERR_INVALID_ARG, "sparse_attn_noalloc: max_pages and num_pages must be >= 1");
+  if (!(sm_scale > 0.f) || sm_scale != sm_scale)
+    return fail(DSA_ERR_INVALID_ARG, "sparse_attn_noalloc: sm_scale must be positive");
+  if (n_q == 0) return DSA_OK;
+  if (!q_bf16 || !kv_cache || !page_table || !seq_lens || !q_seq || !topk_idx || !out_bf16)
+    return fail(DSA_ERR_INVALID_ARG, "sparse_attn_noalloc: null pointer");
+  if (!aligned(q_bf16, 16) || !aligned(kv_cache, 16) || !aligned(out_bf16, 16))
+    return fail(DSA_ERR_INVALID_ARG, "sparse_attn_noalloc: q, kv_cache and out must be 16-byte aligned");
+  const size_t need = dsa::sfa_workspace_bytes(n_q, h_s, topk);
+  if (need > static_cast<size_t>(DSA_NOALLOC_SCRATCH_BYTES))
+    return fail(DSA_ERR_UNSUPPORTED,
+                "sparse_attn_noalloc: n_q=%d, h_s=%d, topk=%d need %zu bytes of scratch, more than the "
+                "fixed %zu (use dsa_sparse_attn with a caller-allocated workspace)",
+                n_q, h_s, topk, need, static_cast<size_t>(DSA_NOALLOC_SCRATCH_BYTES));
+  unsigned* st = status_ptr();
+  if (!st) return fail(DSA_ERR_CUDA, "sparse_attn_noalloc: no CUDA device");
+  dsa::SfaArgs a{q_bf16, n_q, h_s, kv_cache, num_pages, page_table, max_pages, seq_lens, q_seq, n_seq,
+                 topk_idx, topk, sm_scale, out_bf16, out_lse, nullptr, 0, st};
+  const char* why = nullptr;
+  cudaError_t e = dsa::launch_sfa_noalloc(a, static_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess)
+    return why ? fail(DSA_ERR_UNSUPPORTED, "%s", why) : cuda_fail(e, "sparse_attn_noalloc launch");
+  return DSA_OK;
+}
+
 int dsa_device_status(void* stream) {
   unsigned* st = status_ptr();
   if (!st) return fail(DSA_ERR_CUDA, "device_status: no CUDA device");

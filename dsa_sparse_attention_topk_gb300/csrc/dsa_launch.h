@@ -54,5 +54,6 @@ cudaError_t launch_quant_fp8(const void* kv, const int64_t* slots, int n_tokens,
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s, const char** err);
 cudaError_t launch_sfa(const SfaArgs& a, cudaStream_t s, const char** err);
 size_t sfa_workspace_bytes(int n_q, int h_s, int topk);
+cudaError_t launch_sfa_noalloc(const SfaArgs& a, cudaStream_t s, const char** err);
 
 }  // namespace dsa

@@ -32,6 +32,7 @@
 #include <algorithm>
 #include <cfloat>
 #include <cuda.h>
+#include <mutex>
 
 #include "dsa_common.cuh"
 #include "dsa_launch.h"
@@ -522,6 +523,52 @@ cudaError_t launch_sfa(const SfaArgs& a, cudaStream_t s, const char** err) {
   if (e != cudaSuccess || pl.nsplit == 1) return e;
   sfa_combine_kernel<<<dim3(a.n_q, a.h_s), 128, 0, s>>>(a, pl);
   return cudaGetLastError();
+}
+
+// ---- scratch for callers that cannot allocate ----------------------------------------
+// Some callers of this library have no way to allocate device memory for the split-merge
+// workspace: code running under a caching allocator they may not bypass, inside a
+// framework that owns every allocation, or on a path where an allocation call would
+// synchronise the device.  For them the partial outputs go to this fixed array instead.
+// It lives for as long as the library is loaded on a device, is shared by every call on
+// that device, and keeps the last call's contents (nothing in it needs to start at zero:
+// every slot is written before it is read).  Two calls whose kernels overlap on the GPU
+// would race on it.
+static __device__ __align__(256) unsigned char g_sfa_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES];
+
+cudaError_t launch_sfa_noalloc(const SfaArgs& a_in, cudaStream_t s, const char** err) {
+  const size_t need = sfa_workspace_bytes(a_in.n_q, a_in.h_s, a_in.topk);
+  if (need > sizeof(g_sfa_noalloc_scratch)) {
+    *err = "sparse_attn_noalloc: these sizes need more scratch than DSA_NOALLOC_SCRATCH_BYTES";
+    return cudaErrorInvalidValue;
+  }
+  // The host-side name of the array is only a stand-in; the device address comes from
+  // cudaGetSymbolAddress, looked up once per device with that device current.
+  static std::mutex mu;
+  static void* ptrs[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) {
+    *err = "sparse_attn_noalloc: device ordinal out of range";
+    return cudaErrorInvalidDevice;
+  }
+  void* ptr = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+      e = cudaGetSymbolAddress(&ptrs[dev], g_sfa_noalloc_scratch);
+      if (e != cudaSuccess) {
+        ptrs[dev] = nullptr;
+        return e;
+      }
+    }
+    ptr = ptrs[dev];
+  }
+  SfaArgs a = a_in;
+  a.workspace = ptr;
+  a.workspace_bytes = sizeof(g_sfa_noalloc_scratch);
+  return launch_sfa(a, s, err);
 }
 
 }  // namespace dsa

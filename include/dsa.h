@@ -185,6 +185,30 @@ int dsa_sparse_attn(const void* q_bf16, int32_t n_q, int32_t h_s, const uint8_t*
                     float* out_lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * dsa_sparse_attn_noalloc -- dsa_sparse_attn for callers that cannot allocate device
+ * memory.  The pages have no counterpart: this is a convenience of this library.
+ * Some callers have no allocator they may use for the split-merge workspace -- code that
+ * runs under a framework owning every allocation, or on a path where an allocation call
+ * would synchronise the device.  This variant keeps that workspace in one fixed array of
+ * DSA_NOALLOC_SCRATCH_BYTES inside the library, reserved on every GPU that loads the
+ * library until the process exits; it allocates nothing and frees nothing.
+ *   Arguments, outputs and errors are those of dsa_sparse_attn, without the workspace.
+ *   Sizes whose workspace (dsa_sparse_attn_workspace_size) exceeds
+ *   DSA_NOALLOC_SCRATCH_BYTES are rejected with DSA_ERR_UNSUPPORTED and a message.
+ *   The first call on a device looks up the array's device address with that device
+ *   current; make that first call before any stream capture.
+ *   Every call on a device shares the array and it keeps the last call's contents (no
+ *   part of it needs to start at zero).  Calls whose kernels overlap on the GPU -- on
+ *   different streams, or from different threads -- race on it: serialise them.
+ */
+#define DSA_NOALLOC_SCRATCH_BYTES (40u * 1024u * 1024u)
+int dsa_sparse_attn_noalloc(const void* q_bf16, int32_t n_q, int32_t h_s, const uint8_t* kv_cache,
+                            int64_t num_pages, const int32_t* page_table, int32_t max_pages,
+                            const int32_t* seq_lens, const int32_t* q_seq, int32_t n_seq,
+                            const int32_t* topk_idx, int32_t topk, float sm_scale, void* out_bf16,
+                            float* out_lse, void* stream);
+
+/*
  * dsa_device_status -- synchronise `stream`, return the device status word (an OR of
  * DSA_STATUS_* bits recorded by kernels since the last call on this device) and clear
  * it.  Returns a negative DSA_ERR_CUDA if the synchronisation itself failed.
