@@ -16,14 +16,14 @@
 //   warp 0     producer: per 128-position tile, two TMA loads of 64x128 E4M3 page rows
 //              (128-byte swizzle) and two 256-byte bulk loads of the pages' E8M0 scales
 //              into an S-stage shared-memory ring;
-//   warp 1     MMA: transposes the tile's scales into the tcgen05 scale-factor layout,
-//              copies them to TMEM and issues four block-scaled MXFP8 MMAs
-//              (M = 128 positions, N = G * Hp query heads, K = 4 x 32) into a
-//              double-buffered TMEM accumulator;
-//   warps 2-9  epilogue, two sets of four warps (set s drains accumulator s): one TMEM
-//              lane (= one position) per thread, ReLU, head weights and the sum over heads
-//              in registers; the score's order-preserving key goes to shared memory and its
-//              top radix digit into a histogram for the selection.  No score leaves the chip.
+//   MMA warps  (two when N <= 128) each take every other tile: transpose the tile's
+//              scales into the tcgen05 scale-factor layout, copy them to TMEM and issue four
+//              block-scaled MXFP8 MMAs (M = 128 positions, N = G * Hp query heads,
+//              K = 4 x 32) into their own TMEM accumulator;
+//   epilogue   one set of four warps per accumulator: one TMEM lane (= one position) per
+//              thread, ReLU, head weights and the sum over heads in registers; the score's
+//              order-preserving key goes to shared memory and its top radix digit into a
+//              histogram for the selection.  No score leaves the chip.
 // The MXFP8 queries are quantised on chip into the MMA's B operand at kernel start.  After
 // the scan, the cluster selects the Top-K of every row over distributed shared memory
 // (topk_cluster.cuh).
@@ -40,8 +40,17 @@
 namespace dsa {
 namespace {
 
-constexpr int kEpiWarps = 8;           // two sets of four epilogue warps (one per accumulator)
-constexpr int kThreads = 32 * (2 + kEpiWarps);  // 10 warps
+constexpr int kMaxAcc = 2;
+
+// TMEM accumulators per CTA for N = G * HP query-head columns, and as many MMA-issuing
+// warps: accumulator i (tiles t = i mod count) belongs to issuer i and to epilogue set i.
+// A single thread can only issue a tcgen05.mma every ~120-200 cycles whatever N is, so two
+// issuers are needed to keep up with the page stream.  Each barrier that is waited on by
+// parity must see its phases in order from one waiter, which is why an accumulator never
+// moves between issuers and the ring has an even number of stages.
+__host__ __device__ constexpr int acc_count(int np) { return np <= 128 ? 2 : 1; }
+__host__ __device__ constexpr int mma_warps(int np) { return acc_count(np); }
+__host__ __device__ constexpr int threads_for(int np) { return 32 * (1 + mma_warps(np) + 4 * acc_count(np)); }
 constexpr int kTileP = 128;            // positions per MMA tile = two pages
 constexpr int kStageA = kTileP * kIdxDim;        // 16384 B of E4M3 codes
 constexpr int kStageSF = kTileP * 4;             // 512 B of E8M0 scales (position order)
@@ -51,9 +60,9 @@ constexpr int kMaxStages = 8;
 
 struct Plan {
   int G, H, Hp, Np, nacc, stages, chunk_cap;
-  uint32_t tmem_cols, d_col[2], sfa_col[2], sfb_col;
+  uint32_t tmem_cols, d_col[kMaxAcc], sfa_col[kMaxAcc], sfb_col;
   // dynamic shared memory offsets (from a 1024-byte aligned base)
-  uint32_t off_stage, off_b, off_sfb, off_w, off_keys, off_hist0, off_topk, off_bar, total;
+  uint32_t off_stage, off_b, off_sfb, off_w, off_keys, off_hist0, off_pages, off_topk, off_bar, total;
 };
 
 // Query heads padded to the MMA's N granularity: 16, 32 or 64 rows per query row.
@@ -62,8 +71,9 @@ __host__ __device__ constexpr int padded_heads(int h) { return h <= 16 ? 16 : (h
 struct Barriers {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t pages_ready;
+  uint64_t tfull[kMaxAcc];
+  uint64_t tempty[kMaxAcc];
   uint32_t tmem_base;
   int abort;
   int seq;
@@ -79,18 +89,18 @@ __host__ inline Plan make_plan(int G, int H, int chunk_cap, int stages) {
   p.H = H;
   p.Hp = padded_heads(H);
   p.Np = G * p.Hp;
-  p.nacc = p.Np <= 128 ? 2 : 1;
+  p.nacc = acc_count(p.Np);
   p.stages = stages;
   p.chunk_cap = chunk_cap;
-  uint32_t used = p.nacc * p.Np + 16;
+  uint32_t used = p.nacc * p.Np + 4 * p.nacc + 8 * mma_warps(p.Np);
   uint32_t cols = 32;
   while (cols < used) cols *= 2;
   p.tmem_cols = cols;
-  p.d_col[0] = 0;
-  p.d_col[1] = p.Np;
-  p.sfa_col[0] = p.nacc * p.Np;
-  p.sfa_col[1] = p.nacc * p.Np + 4;
-  p.sfb_col = p.nacc * p.Np + 8;
+  for (int i = 0; i < kMaxAcc; ++i) {
+    p.d_col[i] = i * p.Np;
+    p.sfa_col[i] = p.nacc * p.Np + 4 * i;
+  }
+  p.sfb_col = p.nacc * p.Np + 4 * p.nacc;  // issuer i keeps its own copy at sfb_col + 8 i
   uint32_t o = 0;
   p.off_stage = o; o += stages * kStageBytes;
   p.off_b = o = align_up(o, 1024); o += p.Np * kIdxDim;
@@ -98,18 +108,18 @@ __host__ inline Plan make_plan(int G, int H, int chunk_cap, int stages) {
   p.off_w = o; o += 4 * G * p.Hp;
   p.off_keys = o = align_up(o, 16); o += 4u * G * chunk_cap;
   p.off_hist0 = o; o += 4u * G * kHistBins;
+  p.off_pages = o; o += 4u * (chunk_cap / kPage + 2);
   p.off_topk = o = align_up(o, 16); o += sizeof(TopkSmem);
   p.off_bar = o = align_up(o, 16); o += sizeof(Barriers);
   p.total = o;
   return p;
 }
 
-// MXFP8-quantise one 128-wide bf16 row straight into the B operand (128-byte swizzled
-// K-major row n) and return this lane's group exponent code (lanes 0, 8, 16, 24 hold
-// groups 0..3).  Same OCP MX rule as the cache writer.
-__device__ __forceinline__ uint32_t quant_row_to_b(const __nv_bfloat16* src, uint8_t* b_row_base, int n) {
+// MXFP8-quantise one 128-wide bf16 row (this lane's four values, already loaded) straight
+// into the B operand (128-byte swizzled K-major row n) and return this lane's group
+// exponent code (lanes 0, 8, 16, 24 hold groups 0..3).  Same OCP MX rule as the cache writer.
+__device__ __forceinline__ uint32_t quant_row_to_b(uint2 raw, uint8_t* b_row_base, int n) {
   const int lane = threadIdx.x & 31;
-  const uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
   const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
   const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
   float x[4] = {__low2float(a), __high2float(a), __low2float(b), __high2float(b)};
@@ -128,7 +138,7 @@ __device__ __forceinline__ uint32_t quant_row_to_b(const __nv_bfloat16* src, uin
 }
 
 template <int G, int HP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(G * HP), 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan pl) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -146,6 +156,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
   const int row0 = blockIdx.y * G;
   const int H = pl.H, S = pl.stages;
   constexpr int Hp = HP, Np = G * HP;
+  constexpr int kThreads = threads_for(Np), kMma = mma_warps(Np), kNacc = acc_count(Np);
 
   // ---- prologue -------------------------------------------------------------------
   topk_init(tk);
@@ -175,45 +186,16 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
       tc::mbar_init(&bs.full[s], 1);
       tc::mbar_init(&bs.empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    tc::mbar_init(&bs.pages_ready, 32);
+    for (int i = 0; i < kNacc; ++i) {
       tc::mbar_init(&bs.tfull[i], 1);
       tc::mbar_init(&bs.tempty[i], 128);
     }
     tc::mbar_fence_init();
   }
-  if (warp == 0 && lane == 0) tc::prefetch_tmap(&kmap);
-  // B operand: on-chip MXFP8 quantisation of the group's queries (row n = j * Hp + h)
-  for (int n = warp; n < Np; n += kThreads / 32) {
-    const int j = n / Hp, h = n % Hp;
-    uint32_t ecode = 127;
-    if (h < H) {
-      ecode = quant_row_to_b(static_cast<const __nv_bfloat16*>(a.q) + (static_cast<size_t>(row0 + j) * H + h) * kIdxDim,
-                             s_b, n);
-    } else {
-      const int chunk = lane >> 2;
-      *reinterpret_cast<uint32_t*>(s_b + n * 128 + ((chunk ^ (n & 7)) << 4) + (lane & 3) * 4) = 0u;
-    }
-    // gather the four group codes (lanes 0, 8, 16, 24) into one scale word
-    const uint32_t e1 = __shfl_sync(0xffffffffu, ecode, 8), e2 = __shfl_sync(0xffffffffu, ecode, 16),
-                   e3 = __shfl_sync(0xffffffffu, ecode, 24);
-    if (lane == 0) {
-      const uint32_t word = ecode | (e1 << 8) | (e2 << 16) | (e3 << 24);
-      // scale-factor layout: block n/128, row n%32, word (n/32)%4
-      s_sfb[(n >> 7) * 128 + (n & 31) * 4 + ((n >> 5) & 3)] = word;
-    }
-  }
-  // scale words of padding rows up to the end of the last 128-row block
-  for (int n = Np + tid; n < ((Np + 127) / 128) * 128; n += kThreads)
-    s_sfb[(n >> 7) * 128 + (n & 31) * 4 + ((n >> 5) & 3)] = 0x7F7F7F7Fu;
-  for (int i = tid; i < G * Hp; i += kThreads) {
-    const int j = i / Hp, h = i % Hp;
-    s_w[i] = h < H ? a.w[static_cast<size_t>(row0 + j) * H + h] : 0.f;
-  }
   if (warp == 1) tc::tmem_alloc(&bs.tmem_base, pl.tmem_cols);
-  tc::fence_async_smem();
   tc::fence_before_sync();
-  __syncthreads();
-  cluster_sync();  // every CTA of the cluster initialised before any DSMEM traffic
+  __syncthreads();  // barriers, sequence info and the TMEM base are visible to every warp
   tc::fence_after_sync();
 
   const int seq = bs.seq;
@@ -234,16 +216,22 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
     const int pg = ptab[lp];
     return (pg >= 0 && pg < a.num_pages) ? pg : -2;
   };
+  // physical page of each of this chunk's logical pages (-1 past the end, -2 invalid),
+  // looked up once by the producer warp: s_pages[i] belongs to logical page c0/64 + i
+  int32_t* s_pages = reinterpret_cast<int32_t*>(smem + pl.off_pages);
 
   if (warp == 0) {
-    // ---------------- producer ----------------
+    // ---------------- producer: starts streaming pages while the others prepare ----------------
+    for (int i = lane; i < 2 * ntiles; i += 32) s_pages[i] = phys_page(c0 / kPage + i);
+    __syncwarp();
+    tc::mbar_arrive(&bs.pages_ready);
     if (lane == 0) {
+      tc::prefetch_tmap(&kmap);
       for (int t = 0; t < ntiles; ++t) {
         const int s = t % S, it = t / S;
         tc::mbar_wait(&bs.empty[s], (it & 1) ^ 1, abort, a.status);
         uint8_t* st = smem + pl.off_stage + s * kStageBytes;
-        const int lp = (c0 + t * kTileP) / kPage;
-        const int pg0 = phys_page(lp), pg1 = phys_page(lp + 1);
+        const int pg0 = s_pages[2 * t], pg1 = s_pages[2 * t + 1];
         if (pg0 == -2 || pg1 == -2) flag(a.status, DSA_STATUS_BAD_PAGE);
         const uint32_t bytes = (pg0 >= 0 ? (kKPageBytes) : 0) + (pg1 >= 0 ? (kKPageBytes) : 0);
         tc::mbar_arrive_expect_tx(&bs.full[s], bytes);
@@ -259,16 +247,61 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
         }
       }
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+  } else {
+    // ---------------- warps 1..9: B operand, head weights, then MMA / epilogue ----------------
+    // On-chip MXFP8 quantisation of the group's queries (row n = j * Hp + h), with each
+    // warp's row loads issued together before they are used.
+    constexpr int kPrepWarps = kThreads / 32 - 1;
+    constexpr int kBatch = 8;
+    const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(a.q);
+    for (int n0 = warp - 1; n0 < Np; n0 += kPrepWarps * kBatch) {
+      uint2 raw[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int n = n0 + k * kPrepWarps;
+        raw[k] = make_uint2(0u, 0u);
+        if (n < Np && (n % Hp) < H)
+          raw[k] = *reinterpret_cast<const uint2*>(qbase + (static_cast<size_t>(row0 + n / Hp) * H + (n % Hp)) * kIdxDim +
+                                                   4 * lane);
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int n = n0 + k * kPrepWarps;
+        if (n >= Np) break;
+        const uint32_t ecode = quant_row_to_b(raw[k], s_b, n);  // padding rows: zero codes, code 127
+        // gather the four group codes (lanes 0, 8, 16, 24) into one scale word
+        const uint32_t e1 = __shfl_sync(0xffffffffu, ecode, 8), e2 = __shfl_sync(0xffffffffu, ecode, 16),
+                       e3 = __shfl_sync(0xffffffffu, ecode, 24);
+        if (lane == 0) {
+          // scale-factor layout: block n/128, row n%32, word (n/32)%4
+          s_sfb[(n >> 7) * 128 + (n & 31) * 4 + ((n >> 5) & 3)] = ecode | (e1 << 8) | (e2 << 16) | (e3 << 24);
+        }
+      }
+    }
+    // scale words of padding rows up to the end of the last 128-row block
+    for (int n = Np + tid - 32; n < ((Np + 127) / 128) * 128; n += kThreads - 32)
+      s_sfb[(n >> 7) * 128 + (n & 31) * 4 + ((n >> 5) & 3)] = 0x7F7F7F7Fu;
+    for (int i = tid - 32; i < G * Hp; i += kThreads - 32) {
+      const int j = i / Hp, h = i % Hp;
+      s_w[i] = h < H ? a.w[static_cast<size_t>(row0 + j) * H + h] : 0.f;
+    }
+    tc::fence_async_smem();
+    asm volatile("bar.sync 1, %0;" :: "r"(kThreads - 32) : "memory");  // every warp but the producer
+  }
+  if (warp >= 1 && warp <= kMma) {
+    // ---------------- MMA issuers: warp 1 + i takes tiles t = i (mod kMma) ----------------
+    const int mi = warp - 1;
+    const uint32_t sfb = tmem + pl.sfb_col + 8 * mi;
     if (lane == 0) {
-      tc::cp_32x128b_warpx4(tmem + pl.sfb_col, tc::desc_sf_block(smem_u32(s_sfb)));
-      if (Np > 128) tc::cp_32x128b_warpx4(tmem + pl.sfb_col + 4, tc::desc_sf_block(smem_u32(s_sfb + 128)));
+      // each issuer copies the query scale factors to its own columns: its MMAs follow its
+      // own copies in issue order
+      tc::cp_32x128b_warpx4(sfb, tc::desc_sf_block(smem_u32(s_sfb)));
+      if (Np > 128) tc::cp_32x128b_warpx4(sfb + 4, tc::desc_sf_block(smem_u32(s_sfb + 128)));
     }
     const uint64_t bdesc = tc::desc_kmajor_sw128(smem_u32(s_b));
-    for (int t = 0; t < ntiles; ++t) {
+    for (int t = mi; t < ntiles; t += kMma) {
       const int s = t % S, it = t / S;
-      const int acc = t % pl.nacc, ia = t / pl.nacc;
+      const int acc = t % kNacc, ia = t / kNacc;
       uint8_t* st = smem + pl.off_stage + s * kStageBytes;
       tc::mbar_wait(&bs.full[s], it & 1, abort, a.status);
       // scales: position order -> [32 rows][4 words], word (i, j) = position 32 j + i
@@ -287,24 +320,25 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
         const uint64_t adesc = tc::desc_kmajor_sw128(smem_u32(st));
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          tc::mma_mxf8(d, adesc + 2 * k, bdesc + 2 * k, tc::idesc_mxf8_e4m3(Np, k), sfa, tmem + pl.sfb_col, k > 0);
+          tc::mma_mxf8(d, adesc + 2 * k, bdesc + 2 * k, tc::idesc_mxf8_e4m3(Np, k), sfa, sfb, k > 0);
         tc::commit(&bs.empty[s]);
         tc::commit(&bs.tfull[acc]);
       }
       __syncwarp();
     }
-  } else {
-    // ---------------- epilogue (warps 2..9) ----------------
-    const int set = (warp - 2) >> 2;           // which accumulator this warp drains
+  } else if (warp > kMma) {
+    // ---------------- epilogue: set i (four warps) drains accumulator i ----------------
+    const int set = (warp - 1 - kMma) >> 2;    // which accumulator this warp drains
     const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
     const int m = quarter * 32 + lane;         // tile row = position offset in the tile
-    for (int t = set; t < (set < pl.nacc ? ntiles : 0); t += pl.nacc) {
-      const int acc = t % pl.nacc, ia = t / pl.nacc;
+    tc::mbar_wait(&bs.pages_ready, 0, abort, a.status);
+    for (int t = set; t < ntiles; t += kNacc) {
+      const int acc = t % kNacc, ia = t / kNacc;
       const bool ok = tc::mbar_wait(&bs.tfull[acc], ia & 1, abort, a.status);
       tc::fence_after_sync();
       const int local = t * kTileP + m;
       const int p = c0 + local;
-      const bool page_ok = phys_page(p / kPage) >= 0;
+      const bool page_ok = s_pages[local / kPage] >= 0;
       float sc[G];
 #pragma unroll
       for (int j = 0; j < G; ++j) {
@@ -314,10 +348,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
         for (int h0 = 0; h0 < HP; h0 += 16) tc::tmem_ld16(col + h0, reinterpret_cast<uint32_t(&)[16]>(r[h0]));
         tc::tmem_wait_ld();
         const float* wj = s_w + j * HP;
-        float s = 0.f;
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains over the heads
 #pragma unroll
-        for (int h = 0; h < HP; ++h) s = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.f), s);
-        sc[j] = s;
+        for (int h = 0; h < HP; ++h) s4[h & 3] = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.f), s4[h & 3]);
+        sc[j] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
       }
       tc::fence_before_sync();
       tc::mbar_arrive(&bs.tempty[acc]);
@@ -333,6 +367,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
   }
   tc::fence_before_sync();
   __syncthreads();
+  cluster_sync();  // every CTA of the cluster has initialised its selector before DSMEM traffic
 
   if (a.out_idx) {
 #pragma unroll 1
@@ -399,7 +434,7 @@ cudaError_t launch_gh(const IndexerArgs& a, cudaStream_t s, const char** err) {
   while (C < kMaxCluster && make_plan(G, a.h_i, cap_for(C), 4).total > limit) C *= 2;
   while (C < kMaxCluster && static_cast<long long>(n_groups) * C * 2 <= di.n_sm) C *= 2;
   int stages = kMaxStages;
-  while (stages > 2 && make_plan(G, a.h_i, cap_for(C), stages).total > limit) --stages;
+  while (stages > 2 && make_plan(G, a.h_i, cap_for(C), stages).total > limit) stages -= 2;  // even
   const Plan pl = make_plan(G, a.h_i, cap_for(C), stages);
   if (pl.total > limit) {
     *err = "indexer: max_ctx too large for the on-chip score buffer";
@@ -438,7 +473,7 @@ cudaError_t launch_gh(const IndexerArgs& a, cudaStream_t s, const char** err) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, n_groups, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads_for(G * HP), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -13,17 +13,17 @@
 //
 // One CTA handles one query row and one contiguous share ("split") of its selected
 // entries, for all heads at once (M = 128 rows of the MMAs; rows >= h_s are zero):
-//   warp 0      MMA issuer: Q (bf16, 128 x 576, resident, loaded once by TMA) times the
-//               gathered tile (32 entries x 576) -> S in TMEM; then P (bf16) times the
-//               tile's first 512 columns -> O.
+//   warps 0, 5  MMA issuers: Q (bf16, 128 x 576, resident, loaded once by TMA) times the
+//               gathered tile (32 entries x 576) -> S in TMEM (two halves of the K range
+//               into two accumulators); then P (bf16) times the tile's first 512 columns -> O.
 //   warps 1-4   softmax: one head per thread; online softmax in the exp2 domain with a
 //               lazily updated running max (the accumulator is rescaled only when the max
 //               grows by more than 2^8), P written to shared memory as bf16.
-//   warps 5-11  gather: index -> page -> record, 16-byte loads of E4M3 codes, multiply by
+//   warps 6-11  gather: index -> page -> record, 16-byte loads of E4M3 codes, multiply by
 //               the tile scale, bf16 into the 128-byte-swizzled operand tile (double
 //               buffered).  Invalid entries (-1, or past the sequence) become zero rows.
 // TMEM (512 columns): O[:, 0:448] accumulates in columns 0..447.  Columns 448..511 are
-// shared by the S tile (32 columns) and the tile's P V[:, 448:512] product, which the
+// shared by the two S halves (32 columns each) and the tile's P V[:, 448:512] product, which the
 // softmax warps add into register accumulators (so the whole 128 x 512 output fits next
 // to the S tile).
 // Several splits of a row write unnormalised partial outputs with their running max and
@@ -43,8 +43,9 @@ namespace {
 
 constexpr int kTok = 32;                       // selected entries per tile
 constexpr int kSoftWarps = 4;
-constexpr int kGatherWarps = 7;
-constexpr int kThreads = 32 * (1 + kSoftWarps + kGatherWarps);  // 384
+constexpr int kMmaWarpB = 1 + kSoftWarps;       // second MMA issuer (warp 0 is the first)
+constexpr int kGatherWarps = 6;
+constexpr int kThreads = 32 * (2 + kSoftWarps + kGatherWarps);  // 384
 constexpr int kQBlock = 128 * 128;             // one 64-column K-block of Q: 128 rows x 128 B
 constexpr int kQBytes = 9 * kQBlock;           // 147456
 constexpr int kKvBlock = kTok * 128;           // one 64-column K-block of a tile: 4096 B
@@ -92,6 +93,14 @@ struct SfaPlan {
   float* ws_ml;   // [n_q][nsplit][h_s][4] running max (log2 domain), rounded and exact sums
 };
 
+// 2^x with the hardware approximation (relative error ~2^-22; subnormal results flush to
+// zero, which is below what the bf16 weights can hold anyway); 2^-inf = 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -123,11 +132,11 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     tc::mbar_init(&ctl.q_full, 1);
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&ctl.kv_full[b], kGatherWarps);
-      tc::mbar_init(&ctl.kv_empty[b], 1);
+      tc::mbar_init(&ctl.kv_empty[b], 2);
     }
-    tc::mbar_init(&ctl.s_full, 1);
+    tc::mbar_init(&ctl.s_full, 2);
     tc::mbar_init(&ctl.p_full, kSoftWarps);
-    tc::mbar_init(&ctl.pv_done, 1);
+    tc::mbar_init(&ctl.pv_done, 2);
     tc::mbar_init(&ctl.s_free, kSoftWarps);
     tc::mbar_fence_init();
   }
@@ -155,28 +164,37 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     return a.kv_cache + (static_cast<int64_t>(page) * kPage + p % kPage) * kKvTokBytes;
   };
 
-  if (warp == 0) {
-    // ---------------- MMA issuer ----------------
+  if (warp == 0 || warp == kMmaWarpB) {
+    // ---------------- MMA issuers: warp 0 (A) and warp kMmaWarpB (B) ----------------
+    // A single thread can issue a tcgen05.mma only every ~120-200 cycles, whatever N is, so
+    // the tile's MMAs are shared: A takes the first 18 of QK's 36 K-steps into S_a and the
+    // O[:, 0:256] product; B takes the last 18 K-steps into S_b and the O[:, 256:448] and
+    // tail products.  The softmax adds S_a and S_b.
+    const bool isA = warp == 0;
     if (lane == 0) {
-      tc::prefetch_tmap(&qmap);
-      tc::mbar_arrive_expect_tx(&ctl.q_full, kQBytes);
-      for (int kb = 0; kb < 9; ++kb) tc::tma_load_3d(s_q + kb * kQBlock, &qmap, kb * 64, 0, t, &ctl.q_full);
+      if (isA) {
+        tc::prefetch_tmap(&qmap);
+        tc::mbar_arrive_expect_tx(&ctl.q_full, kQBytes);
+        for (int kb = 0; kb < 9; ++kb) tc::tma_load_3d(s_q + kb * kQBlock, &qmap, kb * 64, 0, t, &ctl.q_full);
+      }
       tc::mbar_wait(&ctl.q_full, 0, abort, a.status);
       const uint32_t id_qk = tc::idesc_bf16(kTok, false, false);
       const uint32_t id_v0 = tc::idesc_bf16(256, false, true);
       const uint32_t id_v1 = tc::idesc_bf16(192, false, true);
       const uint32_t id_v2 = tc::idesc_bf16(64, false, true);
+      const uint32_t s_col = isA ? kColS : kColS + kTok;
+      const int step0 = isA ? 0 : 18;
       for (int j = 0; j < nt; ++j) {
         const int b = j & 1;
         uint8_t* kv = s_kv + b * kKvBytes;
         tc::mbar_wait(&ctl.kv_full[b], (j >> 1) & 1, abort, a.status);
         tc::mbar_wait(&ctl.s_free, (j & 1) ^ 1, abort, a.status);
         tc::fence_after_sync();
-        for (int kb = 0; kb < 9; ++kb) {
+        for (int st = step0; st < step0 + 18; ++st) {
+          const int kb = st >> 2, k = st & 3;
           const uint64_t qd = tc::desc_kmajor_sw128(smem_u32(s_q + kb * kQBlock));
           const uint64_t kd = tc::desc_kmajor_sw128(smem_u32(kv + kb * kKvBlock));
-#pragma unroll
-          for (int k = 0; k < 4; ++k) tc::mma_bf16(tmem + kColS, qd + 2 * k, kd + 2 * k, id_qk, (kb | k) != 0);
+          tc::mma_bf16(tmem + s_col, qd + 2 * k, kd + 2 * k, id_qk, st != step0);
         }
         tc::commit(&ctl.s_full);
         tc::mbar_wait(&ctl.p_full, j & 1, abort, a.status);
@@ -185,12 +203,15 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
         for (int ks = 0; ks < 2; ++ks) {
           const uint64_t pd = tc::smem_desc(smem_u32(s_p + ks * 256), 128, 512, 0);
           const uint32_t kofs = ks * 2048;  // 16 entries = two 8-row groups
-          tc::mma_bf16(tmem + 0, pd, tc::smem_desc(smem_u32(kv + 0 * kKvBlock + kofs), kKvBlock, 1024, 2), id_v0,
-                       j > 0 || ks > 0);
-          tc::mma_bf16(tmem + 256, pd, tc::smem_desc(smem_u32(kv + 4 * kKvBlock + kofs), kKvBlock, 1024, 2), id_v1,
-                       j > 0 || ks > 0);
-          tc::mma_bf16(tmem + kColS, pd, tc::smem_desc(smem_u32(kv + 7 * kKvBlock + kofs), kKvBlock, 1024, 2), id_v2,
-                       ks > 0);
+          if (isA) {
+            tc::mma_bf16(tmem + 0, pd, tc::smem_desc(smem_u32(kv + 0 * kKvBlock + kofs), kKvBlock, 1024, 2), id_v0,
+                         j > 0 || ks > 0);
+          } else {
+            tc::mma_bf16(tmem + 256, pd, tc::smem_desc(smem_u32(kv + 4 * kKvBlock + kofs), kKvBlock, 1024, 2), id_v1,
+                         j > 0 || ks > 0);
+            tc::mma_bf16(tmem + kColS, pd, tc::smem_desc(smem_u32(kv + 7 * kKvBlock + kofs), kKvBlock, 1024, 2),
+                         id_v2, ks > 0);
+          }
         }
         tc::commit(&ctl.pv_done);
         tc::commit(&ctl.kv_empty[b]);
@@ -214,19 +235,20 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
       const uint32_t mask = __ballot_sync(0xffffffffu, ctl.valid[j & 1][lane] != 0);
       tc::mbar_wait(&ctl.s_full, j & 1, abort, a.status);
       tc::fence_after_sync();
-      uint32_t sr[32];
+      uint32_t sr[32], sr2[32];
       tc::tmem_ld32(tmem + lane_base + kColS, sr);
+      tc::tmem_ld32(tmem + lane_base + kColS + kTok, sr2);
       tc::tmem_wait_ld();
       float x[32];
       float mt = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        x[i] = ((mask >> i) & 1u) ? __uint_as_float(sr[i]) * c2 : -INFINITY;
+        x[i] = ((mask >> i) & 1u) ? (__uint_as_float(sr[i]) + __uint_as_float(sr2[i])) * c2 : -INFINITY;
         mt = fmaxf(mt, x[i]);
       }
       const bool need = mt > m_ref + kRescaleLog2 || (m_ref == -INFINITY && mt > -INFINITY);
       const float m_new = need ? mt : m_ref;
-      const float alpha = need ? exp2f(m_ref - m_new) : 1.f;  // exp2(-inf) = 0
+      const float alpha = need ? fast_exp2(m_ref - m_new) : 1.f;  // 2^-inf = 0
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         // rescale the TMEM part of this head's accumulator
         for (int c = 0; c < kVLeft; c += 16) {
@@ -248,8 +270,8 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
       float lsum = 0.f, lxsum = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; i += 2) {
-        const float p0 = (m_ref == -INFINITY) ? 0.f : exp2f(x[i] - m_ref);
-        const float p1 = (m_ref == -INFINITY) ? 0.f : exp2f(x[i + 1] - m_ref);
+        const float p0 = (m_ref == -INFINITY) ? 0.f : fast_exp2(x[i] - m_ref);
+        const float p1 = (m_ref == -INFINITY) ? 0.f : fast_exp2(x[i + 1] - m_ref);
         const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
         lsum += __low2float(pb) + __high2float(pb);
         lxsum += p0 + p1;
@@ -344,7 +366,7 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     }
   } else {
     // ---------------- gather + dequantise (warps 5..11) ----------------
-    const int g = tid - 32 * (1 + kSoftWarps);  // 0..223
+    const int g = tid - 32 * (2 + kSoftWarps);  // 0..191
     constexpr int kTasks = kTok * kChunks;       // 1152 chunks of 16 codes per tile
     constexpr int kPer = (kTasks + 32 * kGatherWarps - 1) / (32 * kGatherWarps);  // 6
     // Warm L1 with this split's index list and the sequence's page-table row, so that the

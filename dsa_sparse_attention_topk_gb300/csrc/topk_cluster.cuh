@@ -24,7 +24,7 @@ constexpr int kHistBins = 2048;
 struct TopkSmem {
   uint32_t hist[2][kHistBins];   // leader: cluster histograms (double-buffered)
   uint32_t local[kHistBins];     // every CTA: its histogram of the current digit
-  uint32_t counts[2][16];        // leader: per-rank (count_gt, count_eq)
+  uint32_t counts[2][16];        // every CTA: per-rank (count_gt, count_eq), pushed by each rank
   uint32_t bcast[2];             // every CTA: (digit, count_above) sent by the leader
   uint32_t warp_cnt[2][32];      // per-warp counts for the ordered compaction
 };
@@ -44,14 +44,21 @@ __device__ __forceinline__ void hist_add_top_digit(uint32_t* hist, uint32_t key)
 
 // Leader: find the digit (scanning down from the top bin) where the running count of
 // cl_hist reaches `need`, send (digit, count above it) to every rank, zero cl_hist.
+// One warp: each lane sums a 64-bin slice (lane 0 = the top slice), a shuffle scan finds
+// the slice that crosses `need`, and the warp scans that slice two bins per lane.
 __device__ __forceinline__ void leader_pick(TopkSmem& sm, uint32_t* cl_hist, uint32_t need, uint32_t nrank) {
   const int tid = threadIdx.x;
   if (tid < 32) {
-    const int per = kHistBins / 32;
+    constexpr int per = kHistBins / 32;
     const int lane = tid;
-    const int hi = kHistBins - lane * per;  // lane 0 owns the top slice [hi - per, hi)
+    const int hi = kHistBins - lane * per;  // lane's slice [hi - per, hi)
+    const uint4* h4 = reinterpret_cast<const uint4*>(cl_hist + hi - per);
     uint32_t slice = 0;
-    for (int j = hi - per; j < hi; ++j) slice += cl_hist[j];
+#pragma unroll
+    for (int j = 0; j < per / 4; ++j) {
+      const uint4 v = h4[j];
+      slice += (v.x + v.y) + (v.z + v.w);
+    }
     uint32_t incl = slice;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -60,14 +67,25 @@ __device__ __forceinline__ void leader_pick(TopkSmem& sm, uint32_t* cl_hist, uin
     }
     const uint32_t excl = incl - slice;
     const uint32_t who = __ballot_sync(0xffffffffu, (excl < need) && (need <= incl));
-    if (lane == __ffs(who) - 1) {
-      uint32_t run = excl, found_d = 0, found_above = 0;
-      bool found = false;
-      for (int j = hi - 1; j >= hi - per; --j) {
-        const uint32_t c = cl_hist[j];
-        if (!found && run + c >= need) { found = true; found_d = j; found_above = run; }
-        run += c;
-      }
+    const int src = __ffs(who) - 1;  // the slice holding the crossing (always found)
+    const uint32_t base = __shfl_sync(0xffffffffu, excl, src < 0 ? 0 : src);
+    const int top = kHistBins - (src < 0 ? 0 : src) * per;
+    // bins of that slice in descending order: lane l holds top-1-2l and top-2-2l
+    const uint32_t c0 = cl_hist[top - 1 - 2 * lane], c1 = cl_hist[top - 2 - 2 * lane];
+    const uint32_t pair = c0 + c1;
+    uint32_t pin = pair;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, pin, o);
+      if (lane >= o) pin += v;
+    }
+    const uint32_t above0 = base + pin - pair;          // count above bin top-1-2l
+    const bool hit0 = above0 < need && need <= above0 + c0;
+    const bool hit1 = !hit0 && above0 + c0 < need && need <= above0 + pair;
+    const uint32_t found = __ballot_sync(0xffffffffu, hit0 || hit1);
+    if (src >= 0 && lane == __ffs(found) - 1) {
+      const uint32_t found_d = hit0 ? static_cast<uint32_t>(top - 1 - 2 * lane) : static_cast<uint32_t>(top - 2 - 2 * lane);
+      const uint32_t found_above = hit0 ? above0 : above0 + c0;
       for (uint32_t r = 0; r < nrank; ++r) {
         dsmem_st_u32(dsmem_addr(&sm.bcast[0], r), found_d);
         dsmem_st_u32(dsmem_addr(&sm.bcast[1], r), found_above);
@@ -111,8 +129,6 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, uint32_t* h
 
   uint32_t prefix = 0;
   uint32_t need = static_cast<uint32_t>(K);
-  uint32_t my_gt = 0;   // this CTA's keys above the prefix chosen so far (thread 0's copy)
-  uint32_t my_eq = 0;
 #pragma unroll 1
   for (int lvl = 0; lvl < 3; ++lvl) {
     const int sh = lvl == 0 ? 21 : (lvl == 1 ? 10 : 0);
@@ -122,7 +138,6 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, uint32_t* h
     uint32_t* lh = lvl == 0 ? hist0 : sm.local;
     uint32_t* cl_hist = sm.hist[lvl & 1];
     if (lvl > 0) {
-      __syncthreads();  // thread 0 has finished reading the previous digit's histogram
       for (int i = tid; i < kHistBins; i += nt) sm.local[i] = 0;
       __syncthreads();
       for (int i = tid; i < len; i += nt) {
@@ -138,34 +153,14 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, uint32_t* h
     cluster_sync();
     if (rank == 0) leader_pick(sm, cl_hist, need, nrank);
     cluster_sync();
-    const uint32_t d = sm.bcast[0];
-    prefix |= d << sh;
+    prefix |= sm.bcast[0] << sh;
     need -= sm.bcast[1];
-    // this CTA's keys in digits above d (all of them are selected)
-    if (tid == 0) {
-      for (uint32_t b = d + 1; b <= mask; ++b) my_gt += lh[b];
-      if (lvl == 2) my_eq = lh[d];
-    }
   }
   const uint32_t T = prefix;
   const uint32_t need_eq = need;  // >= 1
 
-  if (tid == 0) {
-    dsmem_st_u32(dsmem_addr(&sm.counts[0][rank], 0), my_gt);
-    dsmem_st_u32(dsmem_addr(&sm.counts[1][rank], 0), my_eq);
-  }
-  cluster_sync();
-  uint32_t gt_before = 0, eq_before = 0, gt_total = 0;
-  for (uint32_t r = 0; r < nrank; ++r) {
-    const uint32_t a = dsmem_ld_u32(dsmem_addr(&sm.counts[0][r], 0));
-    const uint32_t b = dsmem_ld_u32(dsmem_addr(&sm.counts[1][r], 0));
-    if (r < rank) { gt_before += a; eq_before += b; }
-    gt_total += a;
-  }
-  const uint32_t eq_lo = eq_before < need_eq ? eq_before : need_eq;
-  const uint32_t eq_quota = need_eq - eq_lo;  // ties this CTA may still take
-
-  // ordered compaction: warp w owns the contiguous slice [w*span, (w+1)*span)
+  // counts of this CTA's keys above and at T, per warp (warp w owns the contiguous slice
+  // [w*span, (w+1)*span) of the chunk), then per CTA through the leader
   const int span = ((len + nw - 1) / nw + 31) / 32 * 32;
   const int lo = warp * span, hi = min(len, lo + span);
   uint32_t cg = 0, ce = 0;
@@ -177,6 +172,23 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, uint32_t* h
   }
   if (lane == 0) { sm.warp_cnt[0][warp] = cg; sm.warp_cnt[1][warp] = ce; }
   __syncthreads();
+  if (tid < static_cast<int>(nrank)) {  // push this rank's counts into every rank's table
+    uint32_t my_gt = 0, my_eq = 0;
+    for (int w = 0; w < nw; ++w) { my_gt += sm.warp_cnt[0][w]; my_eq += sm.warp_cnt[1][w]; }
+    dsmem_st_u32(dsmem_addr(&sm.counts[0][rank], tid), my_gt);
+    dsmem_st_u32(dsmem_addr(&sm.counts[1][rank], tid), my_eq);
+  }
+  cluster_sync();
+  uint32_t gt_before = 0, eq_before = 0, gt_total = 0;
+  for (uint32_t r = 0; r < nrank; ++r) {
+    const uint32_t a = sm.counts[0][r], b = sm.counts[1][r];
+    if (r < rank) { gt_before += a; eq_before += b; }
+    gt_total += a;
+  }
+  const uint32_t eq_lo = eq_before < need_eq ? eq_before : need_eq;
+  const uint32_t eq_quota = need_eq - eq_lo;  // ties this CTA may still take
+
+  // ordered compaction of each warp's slice
   uint32_t og = gt_before, oe = 0;
   for (int w = 0; w < warp; ++w) { og += sm.warp_cnt[0][w]; oe += sm.warp_cnt[1][w]; }
   const uint32_t lt = (1u << lane) - 1u;

@@ -102,3 +102,27 @@ def test_bad_page_and_length_are_flagged(dsa):
     d.indexer_topk(dw.q_idx, dw.w, dw.k_cache, dw.page_table, dw.seq_lens, qs, dw.q_pos, 64, wl.max_ctx)
     assert d.device_status() & 2
     assert d.device_status() == 0
+
+
+@pytest.mark.slow
+def test_repeated_calls_with_l2_flush_stay_clean(dsa):
+    # Back-to-back launches with cold caches change the relative speed of the pipeline
+    # stages; every bounded wait must still see its barrier phases in order (a timeout
+    # would set the TIMEOUT status bit) and the results must not change.
+    wl = W.make("decode_b32_ctx32k")
+    dw = DeviceWorkload(wl)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    idx0, val0 = dw.indexer_topk()
+    full0 = dw.indexer_scores()
+    out0, _ = dw.sparse_attn(idx0)
+    assert dsa.device_status() == 0
+    for _ in range(15):
+        flush.zero_()
+        idx, val = dw.indexer_topk()
+        flush.zero_()
+        full = dw.indexer_scores()
+        flush.zero_()
+        out, _ = dw.sparse_attn(idx0)
+        assert torch.equal(idx, idx0) and torch.equal(val, val0)
+        assert torch.equal(full, full0) and torch.equal(out, out0)
+    assert dsa.device_status() == 0
