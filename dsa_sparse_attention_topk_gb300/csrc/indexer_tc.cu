@@ -15,7 +15,7 @@
 // select.  Inside a CTA, warps specialise:
 //   warp 0     producer: per 128-position tile, two TMA loads of 64x128 E4M3 page rows
 //              (128-byte swizzle) and two 256-byte bulk loads of the pages' E8M0 scales
-//              into an S-stage shared-memory ring;
+//              into an S-stage shared-memory ring, issued by two lanes in turn;
 //   MMA warps  (two when N <= 128) each take every other tile: transpose the tile's
 //              scales into the tcgen05 scale-factor layout, copy them to TMEM and issue four
 //              block-scaled MXFP8 MMAs (M = 128 positions, N = G * Hp query heads,
@@ -55,6 +55,7 @@ constexpr int kTileP = 128;            // positions per MMA tile = two pages
 constexpr int kStageA = kTileP * kIdxDim;        // 16384 B of E4M3 codes
 constexpr int kStageSF = kTileP * 4;             // 512 B of E8M0 scales (position order)
 constexpr int kStageBytes = kStageA + 2 * kStageSF;  // + transposed copy: 17408 = 17 KB
+constexpr int kProd = 2;              // producer lanes (the ring size is a multiple of it)
 constexpr int kMaxCluster = 16;
 constexpr int kMaxStages = 8;
 
@@ -225,9 +226,11 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
     for (int i = lane; i < 2 * ntiles; i += 32) s_pages[i] = phys_page(c0 / kPage + i);
     __syncwarp();
     tc::mbar_arrive(&bs.pages_ready);
-    if (lane == 0) {
-      tc::prefetch_tmap(&kmap);
-      for (int t = 0; t < ntiles; ++t) {
+    if (lane < kProd) {
+      // lane l issues tiles t = l (mod kProd): one thread alone cannot issue copies fast
+      // enough to keep the HBM busy, and with an even ring each stage keeps one issuer
+      if (lane == 0) tc::prefetch_tmap(&kmap);
+      for (int t = lane; t < ntiles; t += kProd) {
         const int s = t % S, it = t / S;
         tc::mbar_wait(&bs.empty[s], (it & 1) ^ 1, abort, a.status);
         uint8_t* st = smem + pl.off_stage + s * kStageBytes;
@@ -370,11 +373,14 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
   cluster_sync();  // every CTA of the cluster has initialised its selector before DSMEM traffic
 
   if (a.out_idx) {
+    // the copy ring is idle now: it holds the selector's candidate lists
+    uint2* cand = reinterpret_cast<uint2*>(smem + pl.off_stage);
+    const int cand_cap = pl.stages * kStageBytes / static_cast<int>(sizeof(uint2));
 #pragma unroll 1
     for (int j = 0; j < G; ++j) {
       const size_t row = static_cast<size_t>(row0 + j);
-      cluster_topk_row(tk, s_keys + j * pl.chunk_cap, s_hist0 + j * kHistBins, c0, len, bs.n_sel[j], a.topk,
-                       a.out_idx + row * a.topk, a.out_scores ? a.out_scores + row * a.topk : nullptr);
+      cluster_topk_row(tk, s_keys + j * pl.chunk_cap, s_hist0 + j * kHistBins, c0, chunk, len, bs.n_sel[j], a.topk,
+                       a.out_idx + row * a.topk, a.out_scores ? a.out_scores + row * a.topk : nullptr, cand, cand_cap);
     }
   }
   cluster_sync();  // no CTA leaves while its shared memory may still be addressed

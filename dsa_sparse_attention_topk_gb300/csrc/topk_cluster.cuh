@@ -4,13 +4,24 @@
 // in Kimi K3.1 Pro", section 2.1: selection happens on chip, with no intermediate score
 // write-back.  Each CTA of the cluster holds the order-preserving keys of one contiguous
 // chunk of positions in shared memory (key 0 = not selectable).  The K-th largest key T
-// is found by a three-digit radix select (11 + 11 + 10 bits) whose histograms are summed
-// in the leader CTA's shared memory through distributed shared memory.  The first
-// digit's local histogram is built while the scores are produced; the later digits only
-// touch keys that share the selected prefix.  Every CTA then writes its positions with
-// key > T, and the lowest positions with key == T up to K (CTA rank order is position
-// order, so the tie quota is handed out rank by rank).  The output of every CTA is in
-// position order, so the result is deterministic.
+// is found by a three-digit radix select (11 + 11 + 10 bits).
+//
+// First digit: each CTA builds the histogram of its keys' top 11 bits while the scores are
+// produced, adds it into every CTA's copy over distributed shared memory, and after one
+// cluster barrier every CTA picks the digit d0 holding the K-th key on its own.
+//
+// Then, when the keys whose top digit is >= d0 fit in one CTA's (now idle) copy ring, each
+// CTA lists its own such keys with their positions in position order, and after a second
+// barrier the leader pulls the lists in rank order (= position order) and finishes alone:
+// the last two digits over the keys in bin d0, then one ordered pass that writes every
+// key > T and the lowest positions with key == T.  Only block barriers are needed there.
+//
+// Otherwise (a top bin too crowded for the list) the last two digits go through the
+// cluster as well: their histograms are summed in the leader, which broadcasts each digit,
+// and every CTA writes its own keys > T and its share of the ties (CTA rank order is
+// position order, so the tie quota is handed out rank by rank).
+//
+// Either way the output is deterministic: keys > T in position order, then the ties.
 #pragma once
 
 #include "dsa_common.cuh"
@@ -19,17 +30,19 @@ namespace dsa {
 
 constexpr int kHistBins = 2048;
 
-// Shared-memory scratch of the selector (one per CTA; the leader's copy is the
-// cluster-wide one).
+// Shared-memory scratch of the selector (one per CTA).
 struct TopkSmem {
-  uint32_t hist[2][kHistBins];   // leader: cluster histograms (double-buffered)
-  uint32_t local[kHistBins];     // every CTA: its histogram of the current digit
-  uint32_t counts[2][16];        // every CTA: per-rank (count_gt, count_eq), pushed by each rank
-  uint32_t bcast[2];             // every CTA: (digit, count_above) sent by the leader
-  uint32_t warp_cnt[2][32];      // per-warp counts for the ordered compaction
+  uint32_t hist[2][kHistBins];   // [0]: the cluster's first-digit histogram (every CTA);
+                                 // leader: cluster histograms of the later digits
+  uint32_t local[kHistBins];     // this CTA's histogram of the current digit
+  uint32_t counts[2][16];        // per-rank counts
+  uint32_t bcast[2];             // (digit, count_above) sent by the leader
+  uint32_t pick[4];              // results of this CTA's own picks
+  uint32_t warp_cnt[2][32];      // per-warp counts for the ordered compactions
+  uint32_t seg_off[16 * 32 + 1]; // leader: offsets of the (rank, warp) list segments
 };
 
-// Zero the leader's histograms; call before the first cluster_sync of the kernel.
+// Zero the histograms; call before the first cluster_sync of the kernel.
 __device__ __forceinline__ void topk_init(TopkSmem& sm) {
   for (int i = threadIdx.x; i < 2 * kHistBins; i += blockDim.x) (&sm.hist[0][0])[i] = 0;
 }
@@ -42,53 +55,71 @@ __device__ __forceinline__ void hist_add_top_digit(uint32_t* hist, uint32_t key)
   if (key && (__ffs(peers) - 1) == static_cast<int>(threadIdx.x & 31)) atomicAdd(&hist[d], __popc(peers));
 }
 
-// Leader: find the digit (scanning down from the top bin) where the running count of
-// cl_hist reaches `need`, send (digit, count above it) to every rank, zero cl_hist.
-// One warp: each lane sums a 64-bin slice (lane 0 = the top slice), a shuffle scan finds
-// the slice that crosses `need`, and the warp scans that slice two bins per lane.
+// One warp (all 32 lanes): the digit d where the running count of `hist`, scanned down
+// from the top bin, reaches `need`, and the count of the bins above d.  Each lane sums a
+// 64-bin slice (lane 0 = the top slice), a shuffle scan finds the slice that crosses
+// `need`, and the warp scans that slice two bins per lane.  Every lane gets the result;
+// false (and d = above = 0) if the histogram holds fewer than `need`.
+// Not inlined: its call sites run once each, so one shared copy stays warm in the
+// instruction cache.
+__device__ __noinline__ bool warp_pick(const uint32_t* hist, uint32_t need, uint32_t& digit, uint32_t& above) {
+  constexpr int per = kHistBins / 32;
+  const int lane = threadIdx.x & 31;
+  const int hi = kHistBins - lane * per;  // lane's slice [hi - per, hi)
+  const uint4* h4 = reinterpret_cast<const uint4*>(hist + hi - per);
+  uint32_t slice = 0;
+#pragma unroll
+  for (int j = 0; j < per / 4; ++j) {
+    const uint4 v = h4[j];
+    slice += (v.x + v.y) + (v.z + v.w);
+  }
+  uint32_t incl = slice;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const uint32_t excl = incl - slice;
+  const uint32_t who = __ballot_sync(0xffffffffu, (excl < need) && (need <= incl));
+  digit = 0;
+  above = 0;
+  if (!who) return false;
+  const int src = __ffs(who) - 1;
+  const uint32_t base = __shfl_sync(0xffffffffu, excl, src);
+  const int top = kHistBins - src * per;
+  // bins of that slice in descending order: lane l holds top-1-2l and top-2-2l
+  const uint32_t c0 = hist[top - 1 - 2 * lane], c1 = hist[top - 2 - 2 * lane];
+  const uint32_t pair = c0 + c1;
+  uint32_t pin = pair;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, pin, o);
+    if (lane >= o) pin += v;
+  }
+  const uint32_t above0 = base + pin - pair;  // count above bin top-1-2l
+  const bool hit0 = above0 < need && need <= above0 + c0;
+  const bool hit1 = !hit0 && above0 + c0 < need && need <= above0 + pair;
+  const uint32_t found = __ballot_sync(0xffffffffu, hit0 || hit1);
+  if (!found) return false;
+  const int fl = __ffs(found) - 1;
+  const uint32_t d = hit0 ? static_cast<uint32_t>(top - 1 - 2 * lane) : static_cast<uint32_t>(top - 2 - 2 * lane);
+  const uint32_t ab = hit0 ? above0 : above0 + c0;
+  digit = __shfl_sync(0xffffffffu, d, fl);
+  above = __shfl_sync(0xffffffffu, ab, fl);
+  return true;
+}
+
+// Leader: pick on the cluster histogram cl_hist, send (digit, count above it) to every
+// rank, zero cl_hist.
 __device__ __forceinline__ void leader_pick(TopkSmem& sm, uint32_t* cl_hist, uint32_t need, uint32_t nrank) {
   const int tid = threadIdx.x;
   if (tid < 32) {
-    constexpr int per = kHistBins / 32;
-    const int lane = tid;
-    const int hi = kHistBins - lane * per;  // lane's slice [hi - per, hi)
-    const uint4* h4 = reinterpret_cast<const uint4*>(cl_hist + hi - per);
-    uint32_t slice = 0;
-#pragma unroll
-    for (int j = 0; j < per / 4; ++j) {
-      const uint4 v = h4[j];
-      slice += (v.x + v.y) + (v.z + v.w);
-    }
-    uint32_t incl = slice;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    const uint32_t excl = incl - slice;
-    const uint32_t who = __ballot_sync(0xffffffffu, (excl < need) && (need <= incl));
-    const int src = __ffs(who) - 1;  // the slice holding the crossing (always found)
-    const uint32_t base = __shfl_sync(0xffffffffu, excl, src < 0 ? 0 : src);
-    const int top = kHistBins - (src < 0 ? 0 : src) * per;
-    // bins of that slice in descending order: lane l holds top-1-2l and top-2-2l
-    const uint32_t c0 = cl_hist[top - 1 - 2 * lane], c1 = cl_hist[top - 2 - 2 * lane];
-    const uint32_t pair = c0 + c1;
-    uint32_t pin = pair;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, pin, o);
-      if (lane >= o) pin += v;
-    }
-    const uint32_t above0 = base + pin - pair;          // count above bin top-1-2l
-    const bool hit0 = above0 < need && need <= above0 + c0;
-    const bool hit1 = !hit0 && above0 + c0 < need && need <= above0 + pair;
-    const uint32_t found = __ballot_sync(0xffffffffu, hit0 || hit1);
-    if (src >= 0 && lane == __ffs(found) - 1) {
-      const uint32_t found_d = hit0 ? static_cast<uint32_t>(top - 1 - 2 * lane) : static_cast<uint32_t>(top - 2 - 2 * lane);
-      const uint32_t found_above = hit0 ? above0 : above0 + c0;
+    uint32_t d, ab;
+    warp_pick(cl_hist, need, d, ab);
+    if (tid == 0) {
       for (uint32_t r = 0; r < nrank; ++r) {
-        dsmem_st_u32(dsmem_addr(&sm.bcast[0], r), found_d);
-        dsmem_st_u32(dsmem_addr(&sm.bcast[1], r), found_above);
+        dsmem_st_u32(dsmem_addr(&sm.bcast[0], r), d);
+        dsmem_st_u32(dsmem_addr(&sm.bcast[1], r), ab);
       }
     }
   }
@@ -96,15 +127,144 @@ __device__ __forceinline__ void leader_pick(TopkSmem& sm, uint32_t* cl_hist, uin
   for (int i = tid; i < kHistBins; i += blockDim.x) cl_hist[i] = 0;  // ready for reuse
 }
 
+// Block-local pick on this CTA's histogram: (digit, count above) for every thread.
+__device__ __forceinline__ void block_pick(TopkSmem& sm, const uint32_t* hist, uint32_t need, uint32_t& d,
+                                           uint32_t& above) {
+  if (threadIdx.x < 32) {
+    uint32_t dd, ab;
+    warp_pick(hist, need, dd, ab);
+    if (threadIdx.x == 0) { sm.pick[0] = dd; sm.pick[1] = ab; sm.pick[3] = hist[dd]; }
+  }
+  __syncthreads();
+  d = sm.pick[0];
+  above = sm.pick[1];
+}
+
+// Warp w of the block owns the contiguous slice [w*span, (w+1)*span) of n items; span is
+// a multiple of `unit` items.
+__device__ __forceinline__ int warp_span(int n, int unit = 32) {
+  const int nw = blockDim.x >> 5;
+  return ((n + nw - 1) / nw + unit - 1) / unit * unit;
+}
+
+// Leader, after the barrier that publishes every rank's list: warp w of rank r left its
+// keys (in position order) at cand[w*seg .. w*seg + warp_cnt[0][w]) of rank r.  Pull the
+// segments in (rank, warp) order, which is position order, into the compact list
+// cand[list0 ..), finish the selection and write the row.
+__device__ void leader_finish(TopkSmem& sm, uint2* cand, int seg, int list0, int list_cap, uint32_t d0,
+                              uint32_t above0, int K, int32_t* out_idx, float* out_scores) {
+  const uint32_t nrank = cluster_nctarank();
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+  const int nseg = static_cast<int>(nrank) * nw;
+  for (int i = tid; i < nseg; i += nt) {
+    const uint32_t r = static_cast<uint32_t>(i / nw), w = static_cast<uint32_t>(i % nw);
+    const uint32_t c = r == 0 ? sm.warp_cnt[0][w] : dsmem_ld_u32(dsmem_addr(&sm.warp_cnt[0][w], r));
+    sm.seg_off[i + 1] = c < static_cast<uint32_t>(seg) ? c : static_cast<uint32_t>(seg);
+  }
+  __syncthreads();
+  if (warp == 0) {  // inclusive scan of the segment lengths, 32 segments per step
+    uint32_t carry = 0;
+    for (int b0 = 0; b0 < nseg; b0 += 32) {
+      const int i = b0 + lane;
+      uint32_t v = i < nseg ? sm.seg_off[i + 1] : 0u;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      if (i < nseg) sm.seg_off[i + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) sm.seg_off[0] = 0;
+  }
+  __syncthreads();
+  // the histogram bounded the total by list_cap; the clamps only guard inconsistent input
+  const uint32_t n = min(sm.seg_off[nseg], static_cast<uint32_t>(list_cap));
+  uint2* list = cand + list0;
+  for (int i = warp; i < nseg; i += nw) {
+    const uint32_t r = static_cast<uint32_t>(i / nw), w = static_cast<uint32_t>(i % nw);
+    const uint32_t off = sm.seg_off[i], c = sm.seg_off[i + 1] - off;
+    const uint2* src = cand + w * seg;
+    for (uint32_t e = lane; e < c && off + e < n; e += 32)
+      list[off + e] = r == 0 ? src[e] : dsmem_ld_v2(dsmem_addr(&src[e], r));
+  }
+  __syncthreads();
+  cand = list;
+
+  // second and third digits over the keys in bin d0
+  uint32_t need = static_cast<uint32_t>(K) - above0;
+  for (int i = tid; i < kHistBins; i += nt) sm.local[i] = 0;
+  __syncthreads();
+  for (uint32_t v = tid; v < n; v += nt) {
+    const uint32_t k = cand[v].x;
+    if ((k >> 21) == d0) atomicAdd(&sm.local[(k >> 10) & 2047u], 1u);
+  }
+  __syncthreads();
+  uint32_t d1, a1;
+  block_pick(sm, sm.local, need, d1, a1);
+  need -= a1;
+  const uint32_t pre = (d0 << 11) | d1;  // bits 31..10 of T
+  for (int i = tid; i < kHistBins; i += nt) sm.local[i] = 0;
+  __syncthreads();
+  for (uint32_t v = tid; v < n; v += nt) {
+    const uint32_t k = cand[v].x;
+    if ((k >> 10) == pre) atomicAdd(&sm.local[k & 1023u], 1u);
+  }
+  __syncthreads();
+  uint32_t d2, a2;
+  block_pick(sm, sm.local, need, d2, a2);
+  const uint32_t T = (pre << 10) | d2;
+  const uint32_t need_eq = need - a2;                     // >= 1
+  const uint32_t gt_total = static_cast<uint32_t>(K) - need_eq;
+
+  // one ordered pass over the list: keys > T, then the first need_eq keys == T
+  const int span = warp_span(static_cast<int>(n));
+  const int lo = warp * span, hi = min(static_cast<int>(n), lo + span);
+  uint32_t cg = 0, ce = 0;
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    const uint32_t k = i < hi ? cand[i].x : 0u;
+    cg += __popc(__ballot_sync(0xffffffffu, k > T));
+    ce += __popc(__ballot_sync(0xffffffffu, k == T && k != 0u));
+  }
+  if (lane == 0) { sm.warp_cnt[0][warp] = cg; sm.warp_cnt[1][warp] = ce; }
+  __syncthreads();
+  uint32_t og = 0, oe = 0;
+  for (int w = 0; w < warp; ++w) { og += sm.warp_cnt[0][w]; oe += sm.warp_cnt[1][w]; }
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    const uint2 e = i < hi ? cand[i] : make_uint2(0u, 0u);
+    const uint32_t k = e.x;
+    const uint32_t bg = __ballot_sync(0xffffffffu, k > T);
+    const uint32_t be = __ballot_sync(0xffffffffu, k == T && k != 0u);
+    uint32_t slot = 0xFFFFFFFFu;
+    if (k > T) slot = og + __popc(bg & lt);
+    if (k == T && k != 0u) {
+      const uint32_t r = oe + __popc(be & lt);
+      if (r < need_eq) slot = gt_total + r;
+    }
+    if (slot < static_cast<uint32_t>(K)) {  // guards the row against an inconsistent count
+      out_idx[slot] = static_cast<int32_t>(e.y);
+      if (out_scores) out_scores[slot] = key_score(k);
+    }
+    og += __popc(bg);
+    oe += __popc(be);
+  }
+}
+
 // Select the Top-K of one query row.
-//   keys[0..len)  this CTA's keys for positions c0 .. c0+len-1 (0 = not selectable)
-//   hist0         this CTA's histogram of the keys' top digit (bits 31..21); it is
-//                 consumed (left in an unspecified state)
+//   keys[0..len)  this CTA's keys for positions c0 .. c0+len-1 (0 = not selectable);
+//                 16-byte aligned; chunk >= len is the chunk size of every CTA
+//   hist0         this CTA's histogram of the keys' top digit (bits 31..21); read only
 //   n_sel         number of selectable positions of the row (positions 0..n_sel-1)
+//   cand          cand_cap free (key, position) slots of shared memory, at the same offset
+//                 in every CTA of the cluster
 // Writes out_idx[0..K) (and out_scores if non-null).  Must be called by every thread of
-// every CTA of the cluster (it contains cluster barriers).
-__device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, uint32_t* hist0, int c0, int len, int n_sel,
-                                 int K, int32_t* out_idx, float* out_scores) {
+// every CTA of the cluster (it contains cluster barriers).  The caller must pass another
+// cluster barrier before `cand` or the selector's scratch is written again.
+__device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, const uint32_t* hist0, int c0, int chunk, int len,
+                                 int n_sel, int K, int32_t* out_idx, float* out_scores, uint2* cand, int cand_cap) {
   const uint32_t rank = cluster_ctarank();
   const uint32_t nrank = cluster_nctarank();
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
@@ -127,27 +287,78 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, uint32_t* h
     return;
   }
 
-  uint32_t prefix = 0;
-  uint32_t need = static_cast<uint32_t>(K);
+  // ---- first digit: add this CTA's histogram into every CTA's copy, pick locally ----
+  for (int i = tid; i < kHistBins; i += nt) {
+    const uint32_t c = hist0[i];
+    if (c)
+      for (uint32_t r = 0; r < nrank; ++r) dsmem_add_u32(dsmem_addr(&sm.hist[0][i], r), c);
+  }
+  cluster_sync();
+  uint32_t d0, above0;
+  block_pick(sm, sm.hist[0], static_cast<uint32_t>(K), d0, above0);
+  const uint32_t total = above0 + sm.pick[3];  // cluster-wide count of keys with top digit >= d0
+  // every thread has read the picks; the copy is refilled only after a later cluster barrier
+  for (int i = tid; i < kHistBins; i += nt) sm.hist[0][i] = 0;
+
+  // each warp's segment holds up to `seg` entries (its slice of the chunk); the leader's
+  // compact list follows the segments.  `chunk` is the same in every CTA, so is the choice.
+  const int seg = warp_span(chunk, 128);
+  if (nw * seg + static_cast<int>(total) <= cand_cap) {
+    // ---- list this CTA's keys with top digit >= d0, in position order, one pass ----
+    const int lo = warp * seg, hi = min(len, lo + seg);
+    uint2* mine = cand + warp * seg;
+    uint32_t o = 0;
+    for (int base = lo; base < hi; base += 128) {
+      const int i0 = base + 4 * lane;
+      uint4 kv = make_uint4(0u, 0u, 0u, 0u);
+      if (i0 + 3 < hi) {
+        kv = *reinterpret_cast<const uint4*>(keys + i0);
+      } else {
+        if (i0 < hi) kv.x = keys[i0];
+        if (i0 + 1 < hi) kv.y = keys[i0 + 1];
+        if (i0 + 2 < hi) kv.z = keys[i0 + 2];
+      }
+      const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
+      uint32_t cnt = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) cnt += (kk[e] != 0u && (kk[e] >> 21) >= d0) ? 1u : 0u;
+      uint32_t incl = cnt;
+#pragma unroll
+      for (int of = 1; of < 32; of <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, incl, of);
+        if (lane >= of) incl += u;
+      }
+      uint32_t at = o + incl - cnt;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (kk[e] != 0u && (kk[e] >> 21) >= d0) mine[at++] = make_uint2(kk[e], static_cast<uint32_t>(c0 + i0 + e));
+      o += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) sm.warp_cnt[0][warp] = o;
+    cluster_sync();  // every segment and its length is visible to the leader
+    if (rank == 0) leader_finish(sm, cand, seg, nw * seg, cand_cap - nw * seg, d0, above0, K, out_idx, out_scores);
+    return;
+  }
+
+  // ---- crowded top bin: second and third digits through the leader ----
+  uint32_t prefix = d0 << 21;
+  uint32_t need = static_cast<uint32_t>(K) - above0;
 #pragma unroll 1
-  for (int lvl = 0; lvl < 3; ++lvl) {
-    const int sh = lvl == 0 ? 21 : (lvl == 1 ? 10 : 0);
+  for (int lvl = 1; lvl < 3; ++lvl) {
+    const int sh = lvl == 1 ? 10 : 0;
     const int width = lvl == 2 ? 10 : 11;
     const uint32_t mask = (1u << width) - 1u;
     const int hsh = sh + width;  // bits above this digit must equal prefix's
-    uint32_t* lh = lvl == 0 ? hist0 : sm.local;
     uint32_t* cl_hist = sm.hist[lvl & 1];
-    if (lvl > 0) {
-      for (int i = tid; i < kHistBins; i += nt) sm.local[i] = 0;
-      __syncthreads();
-      for (int i = tid; i < len; i += nt) {
-        const uint32_t k = keys[i];
-        if (k != 0u && (k >> hsh) == (prefix >> hsh)) atomicAdd(&sm.local[(k >> sh) & mask], 1u);
-      }
+    for (int i = tid; i < kHistBins; i += nt) sm.local[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < len; i += nt) {
+      const uint32_t k = keys[i];
+      if (k != 0u && (k >> hsh) == (prefix >> hsh)) atomicAdd(&sm.local[(k >> sh) & mask], 1u);
     }
     __syncthreads();
     for (int i = tid; i < kHistBins; i += nt) {
-      const uint32_t c = lh[i];
+      const uint32_t c = sm.local[i];
       if (c) dsmem_add_u32(dsmem_addr(&cl_hist[i], 0), c);
     }
     cluster_sync();
@@ -159,9 +370,8 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, uint32_t* h
   const uint32_t T = prefix;
   const uint32_t need_eq = need;  // >= 1
 
-  // counts of this CTA's keys above and at T, per warp (warp w owns the contiguous slice
-  // [w*span, (w+1)*span) of the chunk), then per CTA through the leader
-  const int span = ((len + nw - 1) / nw + 31) / 32 * 32;
+  // counts of this CTA's keys above and at T, per warp, then per CTA through every rank
+  const int span = warp_span(len);
   const int lo = warp * span, hi = min(len, lo + span);
   uint32_t cg = 0, ce = 0;
   for (int base = lo; base < hi; base += 32) {
@@ -217,7 +427,7 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, uint32_t* h
     og += __popc(bg);
     oe += __popc(be);
   }
-  // keep the leader's counts alive until every rank has read them
+  // keep the counts alive until every rank has read them
   cluster_sync();
 }
 

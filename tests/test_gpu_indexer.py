@@ -102,6 +102,33 @@ def test_all_equal_scores_pick_lowest_positions(dsa):
     assert sorted(idx.cpu().numpy()[0].tolist()) == list(range(K))
 
 
+@pytest.mark.parametrize("n", [40000, 60000])
+def test_crowded_top_bins_with_ties(dsa, n):
+    # keys cycle through 6 values c = 1 + m/8 (m = 0..5: E4M3 codes 256..416 under the
+    # group scale 2^-8, so exact), q = w = 1 over 8 heads, so score = 1024 c exactly.  The
+    # top digit of the scores (sign, exponent, two mantissa bits) puts c = 1.5 and 1.625
+    # in one bin with a third of all keys; only the second digit separates them.  The K
+    # largest are the lowest positions with c = 1.625.  At n = 40000 the keys of that bin
+    # fit the selector's list; at n = 60000 they do not and the last two digits go through
+    # the whole cluster.
+    K = 2048
+    c = 1.0 + (np.arange(n) % 6) / 8.0
+    k = torch.from_numpy(np.repeat(c[:, None], 128, axis=1).astype(np.float32)).to(torch.bfloat16)
+    wl = W.custom([n], h_i=8, topk=K, seed=1)
+    kc = dsa.alloc_k_cache(wl.num_pages)
+    dsa.quant_kv_mxfp8(k.cuda(), torch.from_numpy(wl.slot_mapping(0)).cuda(), kc)
+    q = torch.ones(1, 8, 128, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(1, 8, dtype=torch.float32, device="cuda")
+    vals = torch.empty(1, K, dtype=torch.float32, device="cuda")
+    idx, _ = dsa.indexer_topk(q, w, kc, torch.from_numpy(wl.page_table).cuda(),
+                              torch.tensor([n], dtype=torch.int32, device="cuda"),
+                              torch.zeros(1, dtype=torch.int32, device="cuda"),
+                              torch.tensor([n - 1], dtype=torch.int32, device="cuda"), K, n, out_scores=vals)
+    assert dsa.device_status() == 0
+    assert sorted(idx.cpu().numpy()[0].tolist()) == [5 + 6 * i for i in range(K)]
+    assert np.all(vals.cpu().numpy()[0] == 1024.0 * 1.625)
+
+
 FULL = ["tiny", "decode_b32_ctx32k", "mixed_b128", "long_mtp_b4_ctx128k", "prefill_4k_over_64k"]
 
 
