@@ -12,22 +12,32 @@
 // (576 wide); it is the key and kv[j][0:512] is the value.
 //
 // One CTA handles one query row and one contiguous share ("split") of its selected
-// entries, for all heads at once (M = 128 rows of the MMAs; rows >= h_s are zero):
-//   warps 0, 5  MMA issuers: Q (bf16, 128 x 576, resident, loaded once by TMA) times the
-//               gathered tile (32 entries x 576) -> S in TMEM (two halves of the K range
-//               into two accumulators); then P (bf16) times the tile's first 512 columns -> O.
-//   warps 1-4   softmax: one head per thread; online softmax in the exp2 domain with a
+// entries, for all heads at once (M = 128 rows of the MMAs; rows >= h_s are zero).
+// Sixteen warps, each role in its own warps so that no role's latency sits in another's
+// loop:
+//   warp 0      every Q K^T: Q (bf16, 128 x 576, resident, loaded once by TMA) times a
+//               gathered tile (32 entries x 576) into one of two S buffers in TMEM, so the
+//               next tile's QK^T runs while the softmax works on this one.
+//   warp 1      every P V: O[:, 0:448] into its TMEM accumulator, and O[:, 448:512] in two
+//               32-column rounds through the tile's S buffer (free once its S was read).
+//   warps 4-7   S -> P, one head per thread: online softmax in the exp2 domain with a
 //               lazily updated running max (the accumulator is rescaled only when the max
 //               grows by more than 2^8), P written to shared memory as bf16.
-//   warps 6-11  gather: index -> page -> record, 16-byte loads of E4M3 codes, multiply by
-//               the tile scale, bf16 into the 128-byte-swizzled operand tile (double
-//               buffered).  Invalid entries (-1, or past the sequence) become zero rows.
-// TMEM (512 columns): O[:, 0:448] accumulates in columns 0..447.  Columns 448..511 are
-// shared by the two S halves (32 columns each) and the tile's P V[:, 448:512] product, which the
-// softmax warps add into register accumulators (so the whole 128 x 512 output fits next
-// to the S tile).
+//   warps 8-11  the tail rounds, added into register accumulators (rescaled with the max
+//               that the S -> P warps publish per tile).
+//   warps 2, 3, 12-15  gather: index -> page -> record, 16-byte loads of E4M3 codes,
+//               multiply by the tile scale, bf16 into the 128-byte-swizzled operand tile
+//               (double buffered; the next tile's codes are loaded and converted in
+//               registers before its buffer is free).  Invalid entries (-1, or past the
+//               sequence) become zero rows.
+// TMEM (512 columns): O[:, 0:448] in columns 0..447, S buffers in 448..479 (even tiles)
+// and 480..511 (odd tiles).  At N = 32 an MMA costs ~40 cycles of the SM's operand reads
+// whatever issues it (a 4 KB Q slice and a 1 KB tile slice from shared memory), so QK^T's
+// 36 K-steps per tile set the pace; everything else is arranged to overlap with them.
 // Several splits of a row write unnormalised partial outputs with their running max and
-// sum to the workspace; a small kernel merges them (log-sum-exp weights).
+// sum to the workspace; a small kernel merges them (log-sum-exp weights).  (Merging inside
+// a cluster of the row's splits, through distributed shared memory or through L2, measured
+// slower: the split-merge kernel runs spread over the whole GPU.)
 
 #include <algorithm>
 #include <cfloat>
@@ -42,16 +52,18 @@ namespace dsa {
 namespace {
 
 constexpr int kTok = 32;                       // selected entries per tile
-constexpr int kSoftWarps = 4;
-constexpr int kMmaWarpB = 1 + kSoftWarps;       // second MMA issuer (warp 0 is the first)
-constexpr int kGatherWarps = 6;
-constexpr int kThreads = 32 * (2 + kSoftWarps + kGatherWarps);  // 384
+constexpr int kWarpQK = 0;                     // issues every Q K^T (and the Q load)
+constexpr int kWarpPV = 1;                     // issues every P V
+constexpr int kWarpSoft0 = 4;                  // warps 4..7: S -> P, one TMEM lane quadrant each
+constexpr int kWarpTail0 = 8;                  // warps 8..11: tail rounds, one quadrant each
+constexpr int kGatherWarps = 6;                // warps 2, 3 and 12..15
+constexpr int kThreads = 512;
 constexpr int kQBlock = 128 * 128;             // one 64-column K-block of Q: 128 rows x 128 B
 constexpr int kQBytes = 9 * kQBlock;           // 147456
 constexpr int kKvBlock = kTok * 128;           // one 64-column K-block of a tile: 4096 B
 constexpr int kKvBytes = 9 * kKvBlock;         // 36864
 constexpr int kPBytes = 128 * kTok * 2;        // 8192
-constexpr uint32_t kColS = 448;                // S tile / tail product columns
+constexpr uint32_t kColS = 448;                // S buffers (tile j: kColS + 32 (j & 1)), tail rounds
 constexpr int kVLeft = 448;                    // output columns accumulated in TMEM
 constexpr int kVTail = 64;                     // output columns accumulated in registers
 constexpr int kChunks = kLatent / 16;          // 16-byte code chunks per entry (36)
@@ -59,14 +71,19 @@ constexpr int kSplitTarget = 148;              // CTAs the split count aims for
 constexpr int kMaxSplit = 16;
 constexpr float kRescaleLog2 = 8.0f;           // lazy max update threshold (factor 256)
 
+// Every barrier waited on by parity has waiters that cannot fall two phases behind: each
+// next phase needs something the waiters do after their wait.
 struct Ctl {
   uint64_t q_full;
-  uint64_t kv_full[2];
-  uint64_t kv_empty[2];
-  uint64_t s_full;
-  uint64_t p_full;
-  uint64_t pv_done;
-  uint64_t s_free;
+  uint64_t kv_full[2];     // gather -> everyone: tile in buffer b
+  uint64_t kv_empty[2];    // QK^T and the P V products of the tile are done with buffer b
+  uint64_t s_full[2];      // S of the tile in S buffer b is ready
+  uint64_t s_free[2];      // S buffer b is free again (its tail rounds have been read)
+  uint64_t p_full;         // P of the tile is in shared memory
+  uint64_t p_free;         // every P V product of the tile has completed
+  uint64_t m_ready;        // the tile's running max is in the ring
+  uint64_t tail_full[2];   // a tail round is in S buffer b (two phases per tile)
+  uint64_t tail_empty;     // the first tail round has been read
   uint32_t tmem_base;
   int abort;
   uint8_t valid[2][kTok];  // per KV buffer: selected entry t of the tile is a real cache row
@@ -77,7 +94,10 @@ constexpr uint32_t kOffKv = kQBytes;
 constexpr uint32_t kOffP = kOffKv + 2 * kKvBytes;
 constexpr uint32_t kOffCtl = kOffP + kPBytes;
 constexpr uint32_t kCtlBytes = 256;
-constexpr uint32_t kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + slack for the 1024-byte alignment
+constexpr uint32_t kOffM = kOffCtl + kCtlBytes;  // running max of each head, per tile parity
+constexpr uint32_t kMBytes = 2 * 128 * 4;
+constexpr uint32_t kSmemBytes = kOffM + kMBytes + 1024;  // + slack for the 1024-byte alignment
+static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 
 __host__ __device__ inline int split_count(int n_q, int topk) {
   const int tiles = (topk + kTok - 1) / kTok;
@@ -114,6 +134,7 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
   uint8_t* s_kv = smem + kOffKv;
   uint8_t* s_p = smem + kOffP;
   Ctl& ctl = *reinterpret_cast<Ctl*>(smem + kOffCtl);
+  float* s_m = reinterpret_cast<float*>(smem + kOffM);  // [2][128]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, t = blockIdx.y;
@@ -133,11 +154,14 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&ctl.kv_full[b], kGatherWarps);
       tc::mbar_init(&ctl.kv_empty[b], 2);
+      tc::mbar_init(&ctl.s_full[b], 1);
+      tc::mbar_init(&ctl.s_free[b], 4);
+      tc::mbar_init(&ctl.tail_full[b], 1);
     }
-    tc::mbar_init(&ctl.s_full, 2);
-    tc::mbar_init(&ctl.p_full, kSoftWarps);
-    tc::mbar_init(&ctl.pv_done, 2);
-    tc::mbar_init(&ctl.s_free, kSoftWarps);
+    tc::mbar_init(&ctl.p_full, 4);
+    tc::mbar_init(&ctl.p_free, 1);
+    tc::mbar_init(&ctl.m_ready, 4);
+    tc::mbar_init(&ctl.tail_empty, 4);
     tc::mbar_fence_init();
   }
   if (warp == 0) tc::tmem_alloc(&ctl.tmem_base, 512);
@@ -147,78 +171,85 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
   const uint32_t tmem = ctl.tmem_base;
   volatile int* abort = &ctl.abort;
 
-  // validity of selected entry e of this row (and its cache record)
-  auto record = [&](int e, bool report) -> const uint8_t* {
-    if (e >= a.topk) return nullptr;
-    const int p = idx[e];
-    if (p < 0) return nullptr;
-    if (p >= L || p / kPage >= a.max_pages) {
-      if (report) flag(a.status, DSA_STATUS_BAD_INDEX);
-      return nullptr;
-    }
-    const int page = ptab[p / kPage];
-    if (page < 0 || page >= a.num_pages) {
-      if (report) flag(a.status, DSA_STATUS_BAD_PAGE);
-      return nullptr;
-    }
-    return a.kv_cache + (static_cast<int64_t>(page) * kPage + p % kPage) * kKvTokBytes;
-  };
-
-  if (warp == 0 || warp == kMmaWarpB) {
-    // ---------------- MMA issuers: warp 0 (A) and warp kMmaWarpB (B) ----------------
-    // A single thread can issue a tcgen05.mma only every ~120-200 cycles, whatever N is, so
-    // the tile's MMAs are shared: A takes the first 18 of QK's 36 K-steps into S_a and the
-    // O[:, 0:256] product; B takes the last 18 K-steps into S_b and the O[:, 256:448] and
-    // tail products.  The softmax adds S_a and S_b.
-    const bool isA = warp == 0;
+  if (warp == kWarpQK || warp == kWarpPV) {
+    // ---------------- MMA issuers ----------------
     if (lane == 0) {
-      if (isA) {
+      if (warp == kWarpQK) {
         tc::prefetch_tmap(&qmap);
         tc::mbar_arrive_expect_tx(&ctl.q_full, kQBytes);
         for (int kb = 0; kb < 9; ++kb) tc::tma_load_3d(s_q + kb * kQBlock, &qmap, kb * 64, 0, t, &ctl.q_full);
       }
-      tc::mbar_wait(&ctl.q_full, 0, abort, a.status);
-      const uint32_t id_qk = tc::idesc_bf16(kTok, false, false);
-      const uint32_t id_v0 = tc::idesc_bf16(256, false, true);
-      const uint32_t id_v1 = tc::idesc_bf16(192, false, true);
-      const uint32_t id_v2 = tc::idesc_bf16(64, false, true);
-      const uint32_t s_col = isA ? kColS : kColS + kTok;
-      const int step0 = isA ? 0 : 18;
-      for (int j = 0; j < nt; ++j) {
-        const int b = j & 1;
-        uint8_t* kv = s_kv + b * kKvBytes;
-        tc::mbar_wait(&ctl.kv_full[b], (j >> 1) & 1, abort, a.status);
-        tc::mbar_wait(&ctl.s_free, (j & 1) ^ 1, abort, a.status);
-        tc::fence_after_sync();
-        for (int st = step0; st < step0 + 18; ++st) {
-          const int kb = st >> 2, k = st & 3;
-          const uint64_t qd = tc::desc_kmajor_sw128(smem_u32(s_q + kb * kQBlock));
-          const uint64_t kd = tc::desc_kmajor_sw128(smem_u32(kv + kb * kKvBlock));
-          tc::mma_bf16(tmem + s_col, qd + 2 * k, kd + 2 * k, id_qk, st != step0);
-        }
-        tc::commit(&ctl.s_full);
-        tc::mbar_wait(&ctl.p_full, j & 1, abort, a.status);
-        tc::fence_after_sync();
+    }
+    if (warp == kWarpQK && lane < 2) {
+      // lane l issues the tiles j = l (mod 2): one thread alone issues an MMA only every
+      // ~55-80 cycles, two keep the tensor core's operand reads busy.  Each lane owns one
+      // S buffer and one KV buffer, so every barrier it waits on keeps a single waiter.
+      {
+        const uint32_t id_qk = tc::idesc_bf16(kTok, false, false);
+        tc::mbar_wait(&ctl.q_full, 0, abort, a.status);
+        // descriptors advance by adding (byte offset >> 4) to the start-address field
+        const uint64_t qd0 = tc::desc_kmajor_sw128(smem_u32(s_q));
+        const uint64_t kd0 = tc::desc_kmajor_sw128(smem_u32(s_kv));
+        for (int j = lane; j < nt; j += 2) {
+          // S = Q K^T of tile j into S buffer j & 1
+          const int b = j & 1;
+          tc::mbar_wait(&ctl.kv_full[b], (j >> 1) & 1, abort, a.status);
+          tc::mbar_wait(&ctl.s_free[b], ((j >> 1) & 1) ^ 1, abort, a.status);
+          tc::fence_after_sync();
+          const uint64_t kd = kd0 + static_cast<uint64_t>(b * (kKvBytes >> 4));
+          const uint32_t d = tmem + kColS + kTok * b;
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          const uint64_t pd = tc::smem_desc(smem_u32(s_p + ks * 256), 128, 512, 0);
-          const uint32_t kofs = ks * 2048;  // 16 entries = two 8-row groups
-          if (isA) {
-            tc::mma_bf16(tmem + 0, pd, tc::smem_desc(smem_u32(kv + 0 * kKvBlock + kofs), kKvBlock, 1024, 2), id_v0,
-                         j > 0 || ks > 0);
-          } else {
-            tc::mma_bf16(tmem + 256, pd, tc::smem_desc(smem_u32(kv + 4 * kKvBlock + kofs), kKvBlock, 1024, 2), id_v1,
-                         j > 0 || ks > 0);
-            tc::mma_bf16(tmem + kColS, pd, tc::smem_desc(smem_u32(kv + 7 * kKvBlock + kofs), kKvBlock, 1024, 2),
-                         id_v2, ks > 0);
+          for (int st = 0; st < 36; ++st) {
+            const uint32_t kb = st >> 2, k = st & 3;
+            tc::mma_bf16(d, qd0 + (kb * (kQBlock >> 4) + 2 * k), kd + (kb * (kKvBlock >> 4) + 2 * k), id_qk, st > 0);
           }
+          tc::commit(&ctl.s_full[b]);
+          tc::commit(&ctl.kv_empty[b]);
         }
-        tc::commit(&ctl.pv_done);
-        tc::commit(&ctl.kv_empty[b]);
       }
     }
-  } else if (warp <= kSoftWarps) {
-    // ---------------- softmax (warps 1..4) ----------------
+    if (warp == kWarpPV && lane == 0) {
+      {
+        const uint32_t id_v0 = tc::idesc_bf16(256, false, true);
+        const uint32_t id_v1 = tc::idesc_bf16(192, false, true);
+        const uint32_t id_vt = tc::idesc_bf16(kTok, false, true);
+        for (int j = 0; j < nt; ++j) {
+          // O += P V of tile j; the last 64 output columns go through S buffer j & 1 in two
+          // rounds of 32 that the tail warps add into registers
+          const int b = j & 1;
+          uint8_t* kv = s_kv + b * kKvBytes;
+          tc::mbar_wait(&ctl.kv_full[b], (j >> 1) & 1, abort, a.status);
+          tc::mbar_wait(&ctl.p_full, j & 1, abort, a.status);
+          tc::fence_after_sync();
+          uint64_t pd[2], vd[2];
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            pd[ks] = tc::smem_desc(smem_u32(s_p + ks * 256), 128, 512, 0);
+            vd[ks] = tc::smem_desc(smem_u32(kv + ks * 2048), kKvBlock, 1024, 2);  // 16 entries = two 8-row groups
+          }
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            tc::mma_bf16(tmem + 0, pd[ks], vd[ks], id_v0, j > 0 || ks > 0);
+            tc::mma_bf16(tmem + 256, pd[ks], vd[ks] + 4 * (kKvBlock >> 4), id_v1, j > 0 || ks > 0);
+          }
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            if (r == 1) {
+              tc::mbar_wait(&ctl.tail_empty, j & 1, abort, a.status);
+              tc::fence_after_sync();
+            }
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks)  // columns 448 + 32 r .. : 64 r bytes into the swizzle atom
+              tc::mma_bf16(tmem + kColS + kTok * b, pd[ks], vd[ks] + (7 * (kKvBlock >> 4) + 4 * r), id_vt, ks > 0);
+            tc::commit(&ctl.tail_full[b]);
+          }
+          tc::commit(&ctl.kv_empty[b]);
+          tc::commit(&ctl.p_free);
+        }
+      }
+    }
+  } else if (warp >= kWarpSoft0 && warp < kWarpSoft0 + 4) {
+    // ---------------- S -> P (warps 4..7) ----------------
     const int quarter = warp & 3;
     const int m = quarter * 32 + lane;  // head row
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
@@ -226,31 +257,35 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     // l sums the bf16-rounded weights that the P V product uses (it normalises O);
     // lx sums the unrounded weights (it gives the log-sum-exp)
     float m_ref = -INFINITY, l = 0.f, lx = 0.f;
-    float ot[kVTail];
-#pragma unroll
-    for (int i = 0; i < kVTail; ++i) ot[i] = 0.f;
     for (int j = 0; j < nt; ++j) {
+      const int b = j & 1;
       // the gather warps flag the tile's real entries before they release the buffer
-      tc::mbar_wait(&ctl.kv_full[j & 1], (j >> 1) & 1, abort, a.status);
-      const uint32_t mask = __ballot_sync(0xffffffffu, ctl.valid[j & 1][lane] != 0);
-      tc::mbar_wait(&ctl.s_full, j & 1, abort, a.status);
+      tc::mbar_wait(&ctl.kv_full[b], (j >> 1) & 1, abort, a.status);
+      const uint32_t mask = __ballot_sync(0xffffffffu, ctl.valid[b][lane] != 0);
+      tc::mbar_wait(&ctl.s_full[b], (j >> 1) & 1, abort, a.status);
       tc::fence_after_sync();
-      uint32_t sr[32], sr2[32];
-      tc::tmem_ld32(tmem + lane_base + kColS, sr);
-      tc::tmem_ld32(tmem + lane_base + kColS + kTok, sr2);
+      uint32_t sr[32];
+      tc::tmem_ld32(tmem + lane_base + kColS + kTok * b, sr);
       tc::tmem_wait_ld();
       float x[32];
       float mt = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        x[i] = ((mask >> i) & 1u) ? (__uint_as_float(sr[i]) + __uint_as_float(sr2[i])) * c2 : -INFINITY;
+        x[i] = ((mask >> i) & 1u) ? __uint_as_float(sr[i]) * c2 : -INFINITY;
         mt = fmaxf(mt, x[i]);
       }
       const bool need = mt > m_ref + kRescaleLog2 || (m_ref == -INFINITY && mt > -INFINITY);
       const float m_new = need ? mt : m_ref;
       const float alpha = need ? fast_exp2(m_ref - m_new) : 1.f;  // 2^-inf = 0
+      // the tail warps rescale their part of the accumulator with the same max
+      s_m[b * 128 + m] = m_new;
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&ctl.m_ready);
+      // every P V product of the previous tile has completed: P may be overwritten and the
+      // TMEM accumulator rescaled
+      if (j > 0) tc::mbar_wait(&ctl.p_free, (j - 1) & 1, abort, a.status);
+      tc::fence_after_sync();
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // rescale the TMEM part of this head's accumulator
         for (int c = 0; c < kVLeft; c += 16) {
           uint32_t r[16];
           tc::tmem_ld16(tmem + lane_base + c, r);
@@ -261,8 +296,6 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
         }
         tc::tmem_wait_st();
       }
-#pragma unroll
-      for (int i = 0; i < kVTail; ++i) ot[i] *= alpha;
       l *= alpha;
       lx *= alpha;
       m_ref = m_new;
@@ -288,21 +321,16 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&ctl.p_full);
-      tc::mbar_wait(&ctl.pv_done, j & 1, abort, a.status);
-      tc::fence_after_sync();
-#pragma unroll
-      for (int h = 0; h < kVTail; h += 32) {
-        uint32_t r[32];
-        tc::tmem_ld32(tmem + lane_base + kColS + h, r);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) ot[h + i] += __uint_as_float(r[i]);
-      }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&ctl.s_free);
     }
-    // ---- output: final (one split) or partial (several) ----
+    // every product has completed; hand (max, sums) to the tail warps through the P buffer
+    if (nt > 0) tc::mbar_wait(&ctl.p_free, (nt - 1) & 1, abort, a.status);
+    tc::fence_after_sync();
+    float* s_fin = reinterpret_cast<float*>(s_p);  // [3][128]
+    s_fin[m] = m_ref;
+    s_fin[128 + m] = l;
+    s_fin[256 + m] = lx;
+    asm volatile("bar.sync 1, 256;" ::: "memory");  // S -> P and tail warps
+    // ---- output of columns 0..447 (TMEM): final (one split) or partial (several) ----
     const bool row_ok = m < a.h_s;
     if (pl.nsplit == 1) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -329,16 +357,8 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
           *reinterpret_cast<uint4*>(out + c + 8) = v1;
         }
       }
-      if (row_ok) {
-#pragma unroll
-        for (int c = 0; c < kVTail; c += 8) {
-          *reinterpret_cast<uint4*>(out + kVLeft + c) =
-              make_uint4(pack_bf16(ot[c] * inv, ot[c + 1] * inv), pack_bf16(ot[c + 2] * inv, ot[c + 3] * inv),
-                         pack_bf16(ot[c + 4] * inv, ot[c + 5] * inv), pack_bf16(ot[c + 6] * inv, ot[c + 7] * inv));
-        }
-        if (a.out_lse)
-          a.out_lse[static_cast<size_t>(t) * a.h_s + m] = lx > 0.f ? (m_ref + log2f(lx)) * 0.6931471805599453f : -INFINITY;
-      }
+      if (row_ok && a.out_lse)
+        a.out_lse[static_cast<size_t>(t) * a.h_s + m] = lx > 0.f ? (m_ref + log2f(lx)) * 0.6931471805599453f : -INFINITY;
     } else {
       const size_t slot = (static_cast<size_t>(t) * pl.nsplit + split) * a.h_s + m;
       float* wo = pl.ws_o + slot * kVDim;
@@ -357,93 +377,178 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
             *reinterpret_cast<uint4*>(wo + c + i) = make_uint4(r[i], r[i + 1], r[i + 2], r[i + 3]);
         }
       }
-      if (row_ok) {
+      if (row_ok) *reinterpret_cast<float4*>(pl.ws_ml + 4 * slot) = make_float4(m_ref, l, lx, 0.f);
+    }
+  } else if (warp >= kWarpTail0 && warp < kWarpTail0 + 4) {
+    // ---------------- tail rounds (warps 8..11): output columns 448..511 ----------------
+    const int quarter = warp & 3;
+    const int m = quarter * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    float m_prev = -INFINITY;
+    float ot[kVTail];
+#pragma unroll
+    for (int i = 0; i < kVTail; ++i) ot[i] = 0.f;
+    for (int j = 0; j < nt; ++j) {
+      const int b = j & 1;
+      // the running max the S -> P warps used for this tile: rescale by the same factor
+      tc::mbar_wait(&ctl.m_ready, j & 1, abort, a.status);
+      const float m_new = s_m[b * 128 + m];
+      const float alpha = (m_new == m_prev) ? 1.f : fast_exp2(m_prev - m_new);  // 2^-inf = 0
+      m_prev = m_new;
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int i = 0; i < kVTail; ++i) ot[i] *= alpha;
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        tc::mbar_wait(&ctl.tail_full[b], r, abort, a.status);
+        tc::fence_after_sync();
+        uint32_t rr[32];
+        tc::tmem_ld32(tmem + lane_base + kColS + kTok * b, rr);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ot[32 * r + i] += __uint_as_float(rr[i]);
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(r == 0 ? &ctl.tail_empty : &ctl.s_free[b]);
+      }
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");  // (max, sums) from the S -> P warps
+    const float* s_fin = reinterpret_cast<const float*>(s_p);
+    const float m_ref = s_fin[m], l = s_fin[128 + m], lx = s_fin[256 + m];
+    const bool row_ok = m < a.h_s;
+    if (row_ok) {
+      if (pl.nsplit == 1) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(t) * a.h_s + m) * kVDim;
+#pragma unroll
+        for (int c = 0; c < kVTail; c += 8) {
+          *reinterpret_cast<uint4*>(out + kVLeft + c) =
+              make_uint4(pack_bf16(ot[c] * inv, ot[c + 1] * inv), pack_bf16(ot[c + 2] * inv, ot[c + 3] * inv),
+                         pack_bf16(ot[c + 4] * inv, ot[c + 5] * inv), pack_bf16(ot[c + 6] * inv, ot[c + 7] * inv));
+        }
+      } else {
+        const size_t slot = (static_cast<size_t>(t) * pl.nsplit + split) * a.h_s + m;
+        float* wo = pl.ws_o + slot * kVDim;
 #pragma unroll
         for (int c = 0; c < kVTail; c += 4)
           *reinterpret_cast<float4*>(wo + kVLeft + c) = make_float4(ot[c], ot[c + 1], ot[c + 2], ot[c + 3]);
-        *reinterpret_cast<float4*>(pl.ws_ml + 4 * slot) = make_float4(m_ref, l, lx, 0.f);
       }
     }
+    (void)m_ref;
+    (void)lx;
   } else {
-    // ---------------- gather + dequantise (warps 5..11) ----------------
-    const int g = tid - 32 * (2 + kSoftWarps);  // 0..191
-    constexpr int kTasks = kTok * kChunks;       // 1152 chunks of 16 codes per tile
-    constexpr int kPer = (kTasks + 32 * kGatherWarps - 1) / (32 * kGatherWarps);  // 6
-    // Warm L1 with this split's index list and the sequence's page-table row, so that the
-    // index -> page -> record lookups below are cache hits.
-    {
-      const int e_lo = tile0 * kTok, e_hi = min(a.topk, (tile0 + nt) * kTok);
-      for (int e = e_lo + g * 32; e < e_hi; e += 32 * 32 * kGatherWarps)
-        asm volatile("prefetch.global.L1 [%0];" :: "l"(idx + e));
-      const int npg = min(a.max_pages, (L + kPage - 1) / kPage);
-      for (int pg = g * 32; pg < npg; pg += 32 * 32 * kGatherWarps)
-        asm volatile("prefetch.global.L1 [%0];" :: "l"(ptab + pg));
-    }
-    uint4 code[kPer];
-    float scl[kPer];
-    bool live[kPer];
-    // load the codes of tile jj into the registers (one tile ahead of the conversion)
-    auto load_tile = [&](int jj) {
-      const int e0 = (tile0 + jj) * kTok;
+    // ---------------- gather + dequantise (warps 2, 3, 12..15) ----------------
+    // Thread g owns entry tok = g / 6 of every tile and its 16-byte code chunks
+    // c = s, s + 6, .., s + 30 (s = g % 6): one index -> page -> record lookup per tile, and
+    // six threads read one record's 576 codes in contiguous 96-byte runs.  The loads run
+    // ahead of their use: while tile j is converted, the index entry of tile j + 4, the page
+    // of tile j + 3, an L2 prefetch of the records of tile j + 2 and the codes of tile j + 1
+    // are in flight, so no iteration waits on a load it issued itself and the code loads
+    // find their lines in L2.
+    static_assert(kTok * 6 == 32 * kGatherWarps && kChunks == 36, "six threads per entry, six chunks each");
+    const int g = (warp < 4 ? warp - 2 : warp - 10) * 32 + lane;  // 0..191
+    const int tok = g / 6, s6 = g % 6;
+    const bool reporter = s6 == 0;              // one thread per entry reports bad input
+    auto ld_s32 = [](const int32_t* ptr) {
+      int v;
+      asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(ptr));
+      return v;
+    };
+    // index entry of tile jj for this thread's entry (-1: past the row, or nothing selected)
+    auto entry = [&](int jj) -> int {
+      const int e = (tile0 + jj) * kTok + tok;
+      return (jj < nt && e < a.topk) ? ld_s32(idx + e) : -1;
+    };
+    auto in_range = [&](int p) { return p >= 0 && p < L && p / kPage < a.max_pages; };
+    // physical page of position p (-1 when p is out of range)
+    auto page_of = [&](int p) -> int { return in_range(p) ? ld_s32(ptab + p / kPage) : -1; };
+    uint4 code[6];
+    float scl[6];
+    bool live = false;
+    // request the codes of the entry at position p on page pg
+    auto load_codes = [&](int p, int pg) {
+      live = false;
+      const uint8_t* rec = nullptr;
+      if (p >= 0) {
+        if (!in_range(p)) {
+          if (reporter) flag(a.status, DSA_STATUS_BAD_INDEX);
+        } else if (pg < 0 || pg >= a.num_pages) {
+          if (reporter) flag(a.status, DSA_STATUS_BAD_PAGE);
+        } else {
+          rec = a.kv_cache + (static_cast<int64_t>(pg) * kPage + p % kPage) * kKvTokBytes;
+        }
+      }
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int i = g + k * 32 * kGatherWarps;
-        live[k] = false;
+      for (int k = 0; k < 6; ++k) {
         code[k] = make_uint4(0u, 0u, 0u, 0u);
         scl[k] = 0.f;
-        if (i < kTasks) {
-          const int tok = i / kChunks, c = i % kChunks;
-          const uint8_t* rec = record(e0 + tok, c == 0);
-          if (rec) {
-            live[k] = true;
-            asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(code[k].x), "=r"(code[k].y), "=r"(code[k].z), "=r"(code[k].w)
-                         : "l"(rec + 16 * c));
-            asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];"
-                         : "=f"(scl[k]) : "l"(rec + kKvScaleOff + 4 * (c >> 3)));
-          }
+      }
+      if (rec) {
+        live = true;
+#pragma unroll
+        for (int k = 0; k < 6; ++k) {
+          const int c = s6 + 6 * k;
+          asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(code[k].x), "=r"(code[k].y), "=r"(code[k].z), "=r"(code[k].w)
+                       : "l"(rec + 16 * c));
+          asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];"
+                       : "=f"(scl[k]) : "l"(rec + kKvScaleOff + 4 * (c >> 3)));
         }
       }
     };
-    if (nt > 0) load_tile(0);
+    // pull the record of the entry at position p on page pg towards L2 (the six threads of
+    // the entry take one 128-byte line each; together they cover the 608-byte record)
+    auto prefetch_record = [&](int p, int pg) {
+      if (in_range(p) && pg >= 0 && pg < a.num_pages) {
+        const uint8_t* rec = a.kv_cache + (static_cast<int64_t>(pg) * kPage + p % kPage) * kKvTokBytes;
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(rec + min(128 * s6, kKvTokBytes - 1)));
+      }
+    };
+    // prologue: index entries of tiles 0..3, pages of 0..2, the record of 1 towards L2 and
+    // the codes of tile 0
+    int p1 = entry(0), p2 = entry(1), p3 = entry(2), p4 = entry(3);
+    int pg1 = page_of(p1), pg2 = page_of(p2), pg3 = page_of(p3);
+    prefetch_record(p2, pg2);
+    load_codes(p1, pg1);
+    p1 = p2; pg1 = pg2; p2 = p3; pg2 = pg3; p3 = p4;
     for (int j = 0; j < nt; ++j) {
       const int b = j & 1;
       uint8_t* kv = s_kv + b * kKvBytes;
-      tc::mbar_wait(&ctl.kv_empty[b], ((j >> 1) & 1) ^ 1, abort, a.status);
-      uint4 o0s[kPer], o1s[kPer];
+      // requests for the tiles ahead: the index of j + 4, the page of j + 3 and the record of
+      // j + 2 (towards L2) now, the codes of j + 1 once this tile's have left their registers
+      const int p4n = entry(j + 4);
+      const int pg3n = page_of(p3);
+      prefetch_record(p2, pg2);
+      // this tile's codes -> bf16 in registers
+      uint4 o0s[6], o1s[6];
+      const bool live_j = live;
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        o0s[k] = make_uint4(0u, 0u, 0u, 0u);
-        o1s[k] = o0s[k];
-        if (live[k]) {
-          const uint32_t w[4] = {code[k].x, code[k].y, code[k].z, code[k].w};
-          uint32_t o[8];
+      for (int k = 0; k < 6; ++k) {
+        const uint32_t w[4] = {code[k].x, code[k].y, code[k].z, code[k].w};
+        uint32_t o[8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float f[4];
-            e4m3x4_to_f32(w[q], f);
-            o[2 * q] = pack_bf16(f[0] * scl[k], f[1] * scl[k]);
-            o[2 * q + 1] = pack_bf16(f[2] * scl[k], f[3] * scl[k]);
-          }
-          o0s[k] = make_uint4(o[0], o[1], o[2], o[3]);
-          o1s[k] = make_uint4(o[4], o[5], o[6], o[7]);
+        for (int q = 0; q < 4; ++q) {
+          float f[4];
+          e4m3x4_to_f32(w[q], f);
+          o[2 * q] = pack_bf16(f[0] * scl[k], f[1] * scl[k]);
+          o[2 * q + 1] = pack_bf16(f[2] * scl[k], f[3] * scl[k]);
         }
+        o0s[k] = make_uint4(o[0], o[1], o[2], o[3]);
+        o1s[k] = make_uint4(o[4], o[5], o[6], o[7]);
       }
-      bool flag_live[kPer];
+      load_codes(p1, pg1);
+      p1 = p2; pg1 = pg2; p2 = p3; pg2 = pg3n; p3 = p4n;
+      tc::mbar_wait(&ctl.kv_empty[b], ((j >> 1) & 1) ^ 1, abort, a.status);
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) flag_live[k] = live[k];
-      if (j + 1 < nt) load_tile(j + 1);  // next tile's loads fly while this one is stored
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int i = g + k * 32 * kGatherWarps;
-        if (i >= kTasks) continue;
-        const int tok = i / kChunks, c = i % kChunks;
+      for (int k = 0; k < 6; ++k) {
+        const int c = s6 + 6 * k;
         const int kb = c >> 2, cc = (c & 3) * 2;
         uint8_t* row = kv + kb * kKvBlock + tok * 128;
         *reinterpret_cast<uint4*>(row + ((cc ^ (tok & 7)) << 4)) = o0s[k];
         *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (tok & 7)) << 4)) = o1s[k];
-        if (c == 0) ctl.valid[b][tok] = flag_live[k] ? 1 : 0;
       }
+      if (reporter) ctl.valid[b][tok] = live_j ? 1 : 0;
       tc::fence_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&ctl.kv_full[b]);

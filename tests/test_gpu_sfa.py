@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from dsa_sparse_attention_topk_gb300 import workloads as W
 from dsa_testlib import ensure_built, DeviceWorkload, OracleRows, check_sfa, lse_bound
 
@@ -28,6 +29,10 @@ CASES = {
     "short_ctx": lambda: W.make("short_ctx"),
     "ragged_h100": lambda: W.custom([300, 1, 2500, 129], h_i=16, h_s=100, topk=256, seed=17),
     "mtp_h128": lambda: W.custom([1500, 700], per_seq=2, h_i=16, h_s=128, topk=512, seed=18),
+    # 20 rows -> 7 splits per row, 40 rows -> 3: split counts that do not divide the 512
+    # output columns the cluster's ranks share out
+    "rows20_split7": lambda: W.custom([300 + 37 * i for i in range(20)], h_i=8, h_s=32, topk=256, seed=19),
+    "rows40_split3": lambda: W.custom([200 + 11 * i for i in range(40)], h_i=8, h_s=48, topk=128, seed=20),
 }
 
 
@@ -101,3 +106,34 @@ def test_sfa_full_size_sampled(dsa, name):
         kvh = orc.kv_hat_rows(int(wl.q_seq[r]), idx[r])
         bound = lse_bound(qs[i], kvh, idx[r], wl.sm_scale)
         assert np.all(np.abs(lse.cpu().numpy()[r] - lse_ref) <= bound)
+
+
+def test_every_e4m3_code_dequantises_exactly(dsa):
+    # One selected entry: its softmax weight is exactly 1, so the output row is the
+    # dequantised V row itself.  The row's four 128-wide V tiles hold every non-NaN E4M3
+    # code (positive codes, then negative ones), with the code 448 (0x7E) present so that
+    # each tile's scale amax/448 is the power of two 2^e chosen below; every value
+    # code * 2^e is exact in bf16, so the writer recovers the codes and the expected output
+    # is exact.  Scales 2^-9 and 2^-100 push the subnormal codes' products far down.
+    codes = np.arange(128)
+    codes[0x7F] = 0x7E                      # 0x7F is NaN: use 448 again
+    mag = oracle.codecs.e4m3_decode(codes)
+    tiles = [mag, -mag, mag, -mag]          # codes 0x00..0x7E, then their negatives
+    exps = [0, 5, -9, -100]
+    v = np.concatenate([t * 2.0 ** e for t, e in zip(tiles, exps)] + [np.zeros(64)])
+    wl = W.custom([64], h_i=8, h_s=16, topk=1, seed=3)
+    kv = torch.zeros(64, 576, dtype=torch.float64)
+    kv[5] = torch.from_numpy(v)
+    kv = kv.to(torch.bfloat16)
+    assert torch.equal(kv[5].double(), torch.from_numpy(v))  # exact in bf16
+    kvc = dsa.alloc_kv_cache(wl.num_pages)
+    dsa.quant_kv_fp8(kv.cuda(), torch.from_numpy(wl.slot_mapping(0)).cuda(), kvc)
+    q = torch.randn(1, 16, 576, dtype=torch.float32).to(torch.bfloat16).cuda()
+    idx = torch.tensor([[5]], dtype=torch.int32, device="cuda")
+    out, _ = dsa.sparse_attn(q, kvc, torch.from_numpy(wl.page_table).cuda(),
+                             torch.tensor([64], dtype=torch.int32, device="cuda"),
+                             torch.zeros(1, dtype=torch.int32, device="cuda"), idx, wl.sm_scale)
+    assert dsa.device_status() == 0
+    got = out[0].double().cpu().numpy()
+    want = np.broadcast_to(v[:512], got.shape)
+    assert np.array_equal(got, want), np.argwhere(got != want)[:5]
