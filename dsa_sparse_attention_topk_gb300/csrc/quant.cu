@@ -27,14 +27,15 @@ quant_mxfp8_kernel(const __nv_bfloat16* __restrict__ k, const int64_t* __restric
   const int warp = threadIdx.x >> 5;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp; t < n_tokens;
        t += static_cast<int64_t>(gridDim.x) * kWarpsPerBlock) {
+    // the token's values and its slot are requested together (one memory round trip)
+    const uint2 raw = *reinterpret_cast<const uint2*>(k + t * kIdxDim + 4 * lane);  // dims 4 lane ..
     const int64_t slot = slots[t];
     if (slot < 0) continue;
     if (slot >= num_slots) {
       if (lane == 0) flag(status, DSA_STATUS_BAD_PAGE);
       continue;
     }
-    // lane owns dims 4*lane .. 4*lane+3; group = lane / 8
-    const uint2 raw = *reinterpret_cast<const uint2*>(k + t * kIdxDim + 4 * lane);
+    // group = lane / 8
     const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
     const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
     float x[4] = {__low2float(a), __high2float(a), __low2float(b), __high2float(b)};
@@ -77,18 +78,23 @@ quant_fp8_kernel(const __nv_bfloat16* __restrict__ kv, const int64_t* __restrict
   const int warp = threadIdx.x >> 5;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp; t < n_tokens;
        t += static_cast<int64_t>(gridDim.x) * kWarpsPerBlock) {
+    // every value of the token and its slot are requested together (one memory round trip)
+    const __nv_bfloat16* src = kv + t * kLatent;
+    uint2 raws[4];
+#pragma unroll
+    for (int tile = 0; tile < 4; ++tile) raws[tile] = *reinterpret_cast<const uint2*>(src + tile * 128 + 4 * lane);
+    const __nv_bfloat162 rope = *reinterpret_cast<const __nv_bfloat162*>(src + 512 + 2 * lane);
     const int64_t slot = slots[t];
     if (slot < 0) continue;
     if (slot >= num_slots) {
       if (lane == 0) flag(status, DSA_STATUS_BAD_PAGE);
       continue;
     }
-    const __nv_bfloat16* src = kv + t * kLatent;
     uint8_t* rec = cache + slot * kKvTokBytes;
     float scales[kKvTiles];
 #pragma unroll
     for (int tile = 0; tile < 4; ++tile) {  // four full 128-wide tiles: 4 elements per lane
-      const uint2 raw = *reinterpret_cast<const uint2*>(src + tile * 128 + 4 * lane);
+      const uint2 raw = raws[tile];
       const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
       const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
       float x[4] = {__low2float(a), __high2float(a), __low2float(b), __high2float(b)};
@@ -107,8 +113,7 @@ quant_fp8_kernel(const __nv_bfloat16* __restrict__ kv, const int64_t* __restrict
       scales[tile] = s;
     }
     {  // the 64-wide rope tile: 2 elements per lane
-      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(src + 512 + 2 * lane);
-      float x0 = __low2float(a), x1 = __high2float(a);
+      float x0 = __low2float(rope), x1 = __high2float(rope);
       float amax = fmaxf(fabsf(x0), fabsf(x1));
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));

@@ -24,6 +24,7 @@ class DsaDecodeLayer:
         self.kv_cache = alloc_kv_cache(num_pages, self.device)
         self._ws = {}
         self._bufs = {}
+        self._side = None  # stream for the latent-cache writer of a step
 
     def write(self, k, kv, slot_mapping):
         """Quantise and store new tokens: k bf16 [n, 128], kv bf16 [n, 576], slots int64 [n]."""
@@ -58,6 +59,30 @@ class DsaDecodeLayer:
 
     def step(self, k_new, kv_new, slots_new, q_idx, w, q_sfa, page_table, seq_lens, q_seq, q_pos,
              max_ctx, q_group=1):
-        """Write this step's tokens, then decode."""
-        self.write(k_new, kv_new, slots_new)
-        return self.decode(q_idx, w, q_sfa, page_table, seq_lens, q_seq, q_pos, max_ctx, q_group)
+        """Write this step's tokens, then decode.
+
+        The latent-cache writer only has to finish before sparse attention, so it runs on a
+        second stream alongside the indexer-cache writer and the indexer; the current
+        stream waits for it before sparse attention.
+        """
+        main = torch.cuda.current_stream(self.device)
+        if self._side is None:
+            self._side = torch.cuda.Stream(self.device)
+        side = self._side
+        ready = torch.cuda.Event()
+        ready.record(main)
+        side.wait_event(ready)
+        quant_kv_fp8(kv_new, slots_new, self.kv_cache, stream=side)
+        kv_new.record_stream(side)
+        slots_new.record_stream(side)
+        written = torch.cuda.Event()
+        written.record(side)
+        quant_kv_mxfp8(k_new, slots_new, self.k_cache, stream=main)
+        n_q = q_idx.shape[0]
+        b = self._buffers(n_q)
+        indexer_topk(q_idx, w, self.k_cache, page_table, seq_lens, q_seq, q_pos, self.topk, max_ctx,
+                     q_group=q_group, out_idx=b["idx"], stream=main)
+        main.wait_event(written)
+        sparse_attn(q_sfa, self.kv_cache, page_table, seq_lens, q_seq, b["idx"], self.sm_scale,
+                    out=b["out"], out_lse=b["lse"], workspace=b["ws"], stream=main)
+        return b["out"], b["lse"], b["idx"]
