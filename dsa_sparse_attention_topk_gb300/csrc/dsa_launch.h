@@ -7,6 +7,35 @@
 
 namespace dsa {
 
+// Every kernel of the library is launched with programmatic stream serialization: it may
+// begin (set up shared memory, barriers and TMEM) while the previous kernel on the stream
+// drains, and it waits for that kernel (griddepcontrol.wait, see dsa_common.cuh) before
+// its first global-memory read or write.  cluster_x > 1 adds a cluster dimension.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster_x,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 struct IndexerArgs {
   const void* q;             // bf16 [n_q][h_i][128]
   const float* w;            // [n_q][h_i]

@@ -162,6 +162,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
   // ---- prologue -------------------------------------------------------------------
   topk_init(tk);
   for (int i = tid; i < G * kHistBins; i += kThreads) s_hist0[i] = 0;
+  pdl_launch_dependents();
+  pdl_wait();  // nothing global is touched before the previous kernel on the stream is done
   if (tid == 0) {
     int seq = a.q_seq[row0];
     unsigned bad = 0;
@@ -389,6 +391,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
 }
 
 __global__ void fill_kernel(float* p, size_t n, float v) {
+  pdl_launch_dependents();
+  pdl_wait();
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<size_t>(gridDim.x) * blockDim.x)
     p[i] = v;
@@ -475,21 +479,10 @@ cudaError_t launch_gh(const IndexerArgs& a, cudaStream_t s, const char** err) {
   }
   if (a.out_full) {
     const size_t n = static_cast<size_t>(a.n_q) * a.max_ctx;
-    fill_kernel<<<1024, 256, 0, s>>>(a.out_full, n, -INFINITY);
+    e = launch_pdl(fill_kernel, dim3(1024), dim3(256), 0, s, 1, a.out_full, n, -INFINITY);
+    if (e != cudaSuccess) return e;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, n_groups, 1);
-  cfg.blockDim = dim3(threads_for(G * HP), 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, map, a, pl);
+  return launch_pdl(kern, dim3(C, n_groups, 1), dim3(threads_for(G * HP)), smem, s, C, map, a, pl);
 }
 
 template <int G>

@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 quant_mxfp8_kernel(const __nv_bfloat16* __restrict__ k, const int64_t* __restrict__ slots,
                    int n_tokens, uint8_t* __restrict__ cache, int64_t num_slots,
                    unsigned* status) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp; t < n_tokens;
@@ -74,6 +76,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 quant_fp8_kernel(const __nv_bfloat16* __restrict__ kv, const int64_t* __restrict__ slots,
                  int n_tokens, uint8_t* __restrict__ cache, int64_t num_slots,
                  unsigned* status) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp; t < n_tokens;
@@ -143,17 +147,15 @@ int grid_for(int n_tokens) {
 cudaError_t launch_quant_mxfp8(const void* k, const int64_t* slots, int n_tokens, uint8_t* cache,
                                int64_t num_slots, unsigned* status, cudaStream_t s) {
   if (n_tokens == 0) return cudaSuccess;
-  quant_mxfp8_kernel<<<grid_for(n_tokens), kWarpsPerBlock * 32, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(k), slots, n_tokens, cache, num_slots, status);
-  return cudaGetLastError();
+  return launch_pdl(quant_mxfp8_kernel, dim3(grid_for(n_tokens)), dim3(kWarpsPerBlock * 32), 0, s, 1,
+                    static_cast<const __nv_bfloat16*>(k), slots, n_tokens, cache, num_slots, status);
 }
 
 cudaError_t launch_quant_fp8(const void* kv, const int64_t* slots, int n_tokens, uint8_t* cache,
                              int64_t num_slots, unsigned* status, cudaStream_t s) {
   if (n_tokens == 0) return cudaSuccess;
-  quant_fp8_kernel<<<grid_for(n_tokens), kWarpsPerBlock * 32, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(kv), slots, n_tokens, cache, num_slots, status);
-  return cudaGetLastError();
+  return launch_pdl(quant_fp8_kernel, dim3(grid_for(n_tokens)), dim3(kWarpsPerBlock * 32), 0, s, 1,
+                    static_cast<const __nv_bfloat16*>(kv), slots, n_tokens, cache, num_slots, status);
 }
 
 }  // namespace dsa

@@ -34,8 +34,9 @@
 // and 480..511 (odd tiles).  At N = 32 an MMA costs ~40 cycles of the SM's operand reads
 // whatever issues it (a 4 KB Q slice and a 1 KB tile slice from shared memory), so QK^T's
 // 36 K-steps per tile set the pace; everything else is arranged to overlap with them.
-// Several splits of a row write unnormalised partial outputs with their running max and
-// sum to the workspace; a small kernel merges them (log-sum-exp weights).  (Merging inside
+// Several splits of a row write their partial outputs (each normalised by its own sum,
+// bf16) with their running max and sums to the workspace; a small kernel merges them
+// (log-sum-exp weights).  (Merging inside
 // a cluster of the row's splits, through distributed shared memory or through L2, measured
 // slower: the split-merge kernel runs spread over the whole GPU.)
 
@@ -109,8 +110,8 @@ __host__ __device__ inline int split_count(int n_q, int topk) {
 
 struct SfaPlan {
   int nsplit, tiles_total;
-  float* ws_o;    // [n_q][nsplit][h_s][512] unnormalised partial outputs
-  float* ws_ml;   // [n_q][nsplit][h_s][4] running max (log2 domain), rounded and exact sums
+  __nv_bfloat16* ws_o;  // [n_q][nsplit][h_s][512] partial outputs, each normalised by its own sum l
+  float* ws_ml;         // [n_q][nsplit][h_s][4] running max (log2 domain), rounded and exact sums
 };
 
 // 2^x with the hardware approximation (relative error ~2^-22; subnormal results flush to
@@ -141,14 +142,7 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
   const int tile0 = split * pl.tiles_total / pl.nsplit;
   const int nt = (split + 1) * pl.tiles_total / pl.nsplit - tile0;
 
-  const int seq = a.q_seq[t];
-  const bool seq_ok = seq >= 0 && seq < a.n_seq;
-  const int L = seq_ok ? a.seq_lens[seq] : 0;
-  const int32_t* ptab = a.page_table + static_cast<size_t>(seq_ok ? seq : 0) * a.max_pages;
-  const int32_t* idx = a.idx + static_cast<size_t>(t) * a.topk;
-
   if (tid == 0) {
-    if (!seq_ok && split == 0) flag(a.status, DSA_STATUS_BAD_SEQ);
     ctl.abort = 0;
     tc::mbar_init(&ctl.q_full, 1);
     for (int b = 0; b < 2; ++b) {
@@ -170,6 +164,15 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
   tc::fence_after_sync();
   const uint32_t tmem = ctl.tmem_base;
   volatile int* abort = &ctl.abort;
+
+  pdl_launch_dependents();
+  pdl_wait();  // nothing global is touched before the previous kernel on the stream is done
+  const int seq = a.q_seq[t];
+  const bool seq_ok = seq >= 0 && seq < a.n_seq;
+  const int L = seq_ok ? a.seq_lens[seq] : 0;
+  const int32_t* ptab = a.page_table + static_cast<size_t>(seq_ok ? seq : 0) * a.max_pages;
+  const int32_t* idx = a.idx + static_cast<size_t>(t) * a.topk;
+  if (tid == 0 && !seq_ok && split == 0) flag(a.status, DSA_STATUS_BAD_SEQ);
 
   if (warp == kWarpQK || warp == kWarpPV) {
     // ---------------- MMA issuers ----------------
@@ -330,54 +333,43 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     s_fin[128 + m] = l;
     s_fin[256 + m] = lx;
     asm volatile("bar.sync 1, 256;" ::: "memory");  // S -> P and tail warps
-    // ---- output of columns 0..447 (TMEM): final (one split) or partial (several) ----
+    // ---- columns 0..447 (TMEM), normalised, as bf16: to the output (one split) or to
+    // the workspace (several splits; merged by sfa_combine_kernel) ----
     const bool row_ok = m < a.h_s;
-    if (pl.nsplit == 1) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(t) * a.h_s + m) * kVDim;
-      for (int c = 0; c < kVLeft; c += 16) {
-        uint32_t r[16];
-        if (nt > 0) {
-          tc::tmem_ld16(tmem + lane_base + c, r);
-          tc::tmem_wait_ld();
-        } else {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const size_t slot = (static_cast<size_t>(t) * pl.nsplit + split) * a.h_s + m;
+    __nv_bfloat16* dst = pl.nsplit == 1
+                             ? static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(t) * a.h_s + m) * kVDim
+                             : pl.ws_o + slot * kVDim;
+    for (int c = 0; c < kVLeft; c += 16) {
+      uint32_t r[16];
+      if (nt > 0) {
+        tc::tmem_ld16(tmem + lane_base + c, r);
+        tc::tmem_wait_ld();
+      } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) r[i] = 0u;
-        }
-        if (row_ok) {
-          uint4 v0 = make_uint4(pack_bf16(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv),
-                                pack_bf16(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv),
-                                pack_bf16(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv),
-                                pack_bf16(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv));
-          uint4 v1 = make_uint4(pack_bf16(__uint_as_float(r[8]) * inv, __uint_as_float(r[9]) * inv),
-                                pack_bf16(__uint_as_float(r[10]) * inv, __uint_as_float(r[11]) * inv),
-                                pack_bf16(__uint_as_float(r[12]) * inv, __uint_as_float(r[13]) * inv),
-                                pack_bf16(__uint_as_float(r[14]) * inv, __uint_as_float(r[15]) * inv));
-          *reinterpret_cast<uint4*>(out + c) = v0;
-          *reinterpret_cast<uint4*>(out + c + 8) = v1;
-        }
+        for (int i = 0; i < 16; ++i) r[i] = 0u;
       }
-      if (row_ok && a.out_lse)
-        a.out_lse[static_cast<size_t>(t) * a.h_s + m] = lx > 0.f ? (m_ref + log2f(lx)) * 0.6931471805599453f : -INFINITY;
-    } else {
-      const size_t slot = (static_cast<size_t>(t) * pl.nsplit + split) * a.h_s + m;
-      float* wo = pl.ws_o + slot * kVDim;
-      for (int c = 0; c < kVLeft; c += 16) {
-        uint32_t r[16];
-        if (nt > 0) {
-          tc::tmem_ld16(tmem + lane_base + c, r);
-          tc::tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) r[i] = 0u;
-        }
-        if (row_ok) {
-#pragma unroll
-          for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<uint4*>(wo + c + i) = make_uint4(r[i], r[i + 1], r[i + 2], r[i + 3]);
-        }
+      if (row_ok) {
+        uint4 v0 = make_uint4(pack_bf16(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv),
+                              pack_bf16(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv),
+                              pack_bf16(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv),
+                              pack_bf16(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv));
+        uint4 v1 = make_uint4(pack_bf16(__uint_as_float(r[8]) * inv, __uint_as_float(r[9]) * inv),
+                              pack_bf16(__uint_as_float(r[10]) * inv, __uint_as_float(r[11]) * inv),
+                              pack_bf16(__uint_as_float(r[12]) * inv, __uint_as_float(r[13]) * inv),
+                              pack_bf16(__uint_as_float(r[14]) * inv, __uint_as_float(r[15]) * inv));
+        *reinterpret_cast<uint4*>(dst + c) = v0;
+        *reinterpret_cast<uint4*>(dst + c + 8) = v1;
       }
-      if (row_ok) *reinterpret_cast<float4*>(pl.ws_ml + 4 * slot) = make_float4(m_ref, l, lx, 0.f);
+    }
+    if (row_ok) {
+      if (pl.nsplit == 1) {
+        if (a.out_lse)
+          a.out_lse[static_cast<size_t>(t) * a.h_s + m] = lx > 0.f ? (m_ref + log2f(lx)) * 0.6931471805599453f : -INFINITY;
+      } else {
+        *reinterpret_cast<float4*>(pl.ws_ml + 4 * slot) = make_float4(m_ref, l, lx, 0.f);
+      }
     }
   } else if (warp >= kWarpTail0 && warp < kWarpTail0 + 4) {
     // ---------------- tail rounds (warps 8..11): output columns 448..511 ----------------
@@ -418,21 +410,15 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     const float m_ref = s_fin[m], l = s_fin[128 + m], lx = s_fin[256 + m];
     const bool row_ok = m < a.h_s;
     if (row_ok) {
-      if (pl.nsplit == 1) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(t) * a.h_s + m) * kVDim;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* dst = pl.nsplit == 1
+                               ? static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(t) * a.h_s + m) * kVDim
+                               : pl.ws_o + ((static_cast<size_t>(t) * pl.nsplit + split) * a.h_s + m) * kVDim;
 #pragma unroll
-        for (int c = 0; c < kVTail; c += 8) {
-          *reinterpret_cast<uint4*>(out + kVLeft + c) =
-              make_uint4(pack_bf16(ot[c] * inv, ot[c + 1] * inv), pack_bf16(ot[c + 2] * inv, ot[c + 3] * inv),
-                         pack_bf16(ot[c + 4] * inv, ot[c + 5] * inv), pack_bf16(ot[c + 6] * inv, ot[c + 7] * inv));
-        }
-      } else {
-        const size_t slot = (static_cast<size_t>(t) * pl.nsplit + split) * a.h_s + m;
-        float* wo = pl.ws_o + slot * kVDim;
-#pragma unroll
-        for (int c = 0; c < kVTail; c += 4)
-          *reinterpret_cast<float4*>(wo + kVLeft + c) = make_float4(ot[c], ot[c + 1], ot[c + 2], ot[c + 3]);
+      for (int c = 0; c < kVTail; c += 8) {
+        *reinterpret_cast<uint4*>(dst + kVLeft + c) =
+            make_uint4(pack_bf16(ot[c] * inv, ot[c + 1] * inv), pack_bf16(ot[c + 2] * inv, ot[c + 3] * inv),
+                       pack_bf16(ot[c + 4] * inv, ot[c + 5] * inv), pack_bf16(ot[c + 6] * inv, ot[c + 7] * inv));
       }
     }
     (void)m_ref;
@@ -505,6 +491,15 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
         asm volatile("prefetch.global.L2 [%0];" :: "l"(rec + min(128 * s6, kKvTokBytes - 1)));
       }
     };
+    // warm L2 with this split's index entries and the sequence's page-table row (one
+    // 128-byte line per thread), so that the first lookups do not each pay a DRAM access
+    {
+      const int e_lo = tile0 * kTok, e_hi = min(a.topk, (tile0 + nt) * kTok);
+      const int npg = min(a.max_pages, (L + kPage - 1) / kPage);
+      if (e_lo + 32 * g < e_hi) asm volatile("prefetch.global.L2 [%0];" :: "l"(idx + e_lo + 32 * g));
+      for (int i = 32 * g; i < npg; i += 32 * 32 * kGatherWarps)
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(ptab + i));
+    }
     // prologue: index entries of tiles 0..3, pages of 0..2, the record of 1 towards L2 and
     // the codes of tile 0
     int p1 = entry(0), p2 = entry(1), p3 = entry(2), p4 = entry(3);
@@ -560,28 +555,35 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
-// Merge the splits of each (row, head): weights 2^(m_s - M), M = max_s m_s.
+// Merge the splits of each (row, head).  Split s holds O_s / l_s with running max m_s; with
+// M = max_s m_s and c_s = 2^(m_s - M) l_s the output is sum_s c_s (O_s / l_s) / sum_s c_s.
 __global__ void __launch_bounds__(128)
 sfa_combine_kernel(SfaArgs a, SfaPlan pl) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int t = blockIdx.x, h = blockIdx.y;
   const int ns = pl.nsplit;
   float M = -INFINITY;
   for (int s = 0; s < ns; ++s) M = fmaxf(M, pl.ws_ml[4 * ((static_cast<size_t>(t) * ns + s) * a.h_s + h)]);
-  float wsum = 0.f, wsum_x = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float csum = 0.f, wsum_x = 0.f;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int s = 0; s < ns; ++s) {
     const size_t slot = (static_cast<size_t>(t) * ns + s) * a.h_s + h;
     const float4 ml = *reinterpret_cast<const float4*>(pl.ws_ml + 4 * slot);
     const float wgt = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-    wsum += wgt * ml.y;
+    const float c = wgt * ml.y;
+    csum += c;
     wsum_x += wgt * ml.z;
-    const float4 v = *reinterpret_cast<const float4*>(pl.ws_o + slot * kVDim + 4 * threadIdx.x);
-    acc.x += wgt * v.x; acc.y += wgt * v.y; acc.z += wgt * v.z; acc.w += wgt * v.w;
+    const uint2 v = *reinterpret_cast<const uint2*>(pl.ws_o + slot * kVDim + 4 * threadIdx.x);
+    const __nv_bfloat162 v01 = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
+    const __nv_bfloat162 v23 = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
+    acc[0] += c * __low2float(v01); acc[1] += c * __high2float(v01);
+    acc[2] += c * __low2float(v23); acc[3] += c * __high2float(v23);
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const float inv = csum > 0.f ? 1.f / csum : 0.f;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(t) * a.h_s + h) * kVDim;
   *reinterpret_cast<uint2*>(out + 4 * threadIdx.x) =
-      make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+      make_uint2(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv));
   if (a.out_lse && threadIdx.x == 0)
     a.out_lse[static_cast<size_t>(t) * a.h_s + h] =
         wsum_x > 0.f ? (M + log2f(wsum_x)) * 0.6931471805599453f : -INFINITY;
@@ -604,7 +606,7 @@ EncodeFn encode_fn() {
 }
 
 size_t ws_o_bytes(int n_q, int h_s, int ns) {
-  return (static_cast<size_t>(n_q) * ns * h_s * kVDim * sizeof(float) + 255) / 256 * 256;
+  return (static_cast<size_t>(n_q) * ns * h_s * kVDim * sizeof(__nv_bfloat16) + 255) / 256 * 256;
 }
 
 }  // namespace
@@ -621,7 +623,7 @@ cudaError_t launch_sfa(const SfaArgs& a, cudaStream_t s, const char** err) {
   pl.nsplit = split_count(a.n_q, a.topk);
   pl.tiles_total = (a.topk + kTok - 1) / kTok;
   if (pl.nsplit > 1) {
-    pl.ws_o = static_cast<float*>(a.workspace);
+    pl.ws_o = static_cast<__nv_bfloat16*>(a.workspace);
     pl.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + ws_o_bytes(a.n_q, a.h_s, pl.nsplit));
   }
   EncodeFn enc = encode_fn();
@@ -645,11 +647,9 @@ cudaError_t launch_sfa(const SfaArgs& a, cudaStream_t s, const char** err) {
   cudaError_t e = cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  sfa_tc_kernel<<<dim3(pl.nsplit, a.n_q), kThreads, kSmemBytes, s>>>(qmap, a, pl);
-  e = cudaGetLastError();
+  e = launch_pdl(sfa_tc_kernel, dim3(pl.nsplit, a.n_q), dim3(kThreads), kSmemBytes, s, 1, qmap, a, pl);
   if (e != cudaSuccess || pl.nsplit == 1) return e;
-  sfa_combine_kernel<<<dim3(a.n_q, a.h_s), 128, 0, s>>>(a, pl);
-  return cudaGetLastError();
+  return launch_pdl(sfa_combine_kernel, dim3(a.n_q, a.h_s), dim3(128), 0, s, 1, a, pl);
 }
 
 // ---- scratch for callers that cannot allocate ----------------------------------------

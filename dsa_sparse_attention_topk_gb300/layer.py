@@ -61,9 +61,9 @@ class DsaDecodeLayer:
              max_ctx, q_group=1):
         """Write this step's tokens, then decode.
 
-        The latent-cache writer only has to finish before sparse attention, so it runs on a
-        second stream alongside the indexer-cache writer and the indexer; the current
-        stream waits for it before sparse attention.
+        The latent-cache writer runs on a second stream beside the indexer-cache writer; the
+        current stream joins it before the indexer, so that the indexer and sparse attention
+        follow each other directly (the library launches with programmatic dependent launch).
         """
         main = torch.cuda.current_stream(self.device)
         if self._side is None:
@@ -78,11 +78,11 @@ class DsaDecodeLayer:
         written = torch.cuda.Event()
         written.record(side)
         quant_kv_mxfp8(k_new, slots_new, self.k_cache, stream=main)
+        main.wait_event(written)
         n_q = q_idx.shape[0]
         b = self._buffers(n_q)
         indexer_topk(q_idx, w, self.k_cache, page_table, seq_lens, q_seq, q_pos, self.topk, max_ctx,
                      q_group=q_group, out_idx=b["idx"], stream=main)
-        main.wait_event(written)
         sparse_attn(q_sfa, self.kv_cache, page_table, seq_lens, q_seq, b["idx"], self.sm_scale,
                     out=b["out"], out_lse=b["lse"], workspace=b["ws"], stream=main)
         return b["out"], b["lse"], b["idx"]
