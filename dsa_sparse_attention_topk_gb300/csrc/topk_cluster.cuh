@@ -10,18 +10,19 @@
 // produced, adds it into every CTA's copy over distributed shared memory, and after one
 // cluster barrier every CTA picks the digit d0 holding the K-th key on its own.
 //
-// Then, when the keys whose top digit is >= d0 fit in one CTA's (now idle) copy ring, each
-// CTA lists its own such keys with their positions in position order, and after a second
-// barrier the leader pulls the lists in rank order (= position order) and finishes alone:
-// the last two digits over the keys in bin d0, then one ordered pass that writes every
-// key > T and the lowest positions with key == T.  Only block barriers are needed there.
+// Then, when the keys of bin d0 fit in one CTA's (now idle) copy ring, every CTA counts its
+// keys above bin d0 and in it, and the counts are exchanged (second barrier).  Each CTA
+// writes its keys above d0 straight to the output at its rank's offset, and its keys in
+// bin d0 with their positions into the leader's list at its rank's offset, both in
+// position order (third barrier).  The leader finishes alone over those few candidates:
+// the last two digits, then the keys > T and the lowest positions with key == T.
 //
 // Otherwise (a top bin too crowded for the list) the last two digits go through the
 // cluster as well: their histograms are summed in the leader, which broadcasts each digit,
 // and every CTA writes its own keys > T and its share of the ties (CTA rank order is
 // position order, so the tie quota is handed out rank by rank).
 //
-// Either way the output is deterministic: keys > T in position order, then the ties.
+// Either way the output is deterministic.
 #pragma once
 
 #include "dsa_common.cuh"
@@ -62,15 +63,17 @@ __device__ __forceinline__ void hist_add_top_digit(uint32_t* hist, uint32_t key)
 // false (and d = above = 0) if the histogram holds fewer than `need`.
 // Not inlined: its call sites run once each, so one shared copy stays warm in the
 // instruction cache.
-__device__ __noinline__ bool warp_pick(const uint32_t* hist, uint32_t need, uint32_t& digit, uint32_t& above) {
+__device__ __noinline__ uint3 warp_pick_impl(const uint32_t* hist, uint32_t need) {
   constexpr int per = kHistBins / 32;
   const int lane = threadIdx.x & 31;
   const int hi = kHistBins - lane * per;  // lane's slice [hi - per, hi)
   const uint4* h4 = reinterpret_cast<const uint4*>(hist + hi - per);
   uint32_t slice = 0;
+  // lane l starts l vectors into its slice: the warp's 32 loads of each step then spread
+  // over the banks (slices are 256 bytes apart, so a common order would conflict 32-way)
 #pragma unroll
   for (int j = 0; j < per / 4; ++j) {
-    const uint4 v = h4[j];
+    const uint4 v = h4[(j + lane) & (per / 4 - 1)];
     slice += (v.x + v.y) + (v.z + v.w);
   }
   uint32_t incl = slice;
@@ -81,9 +84,7 @@ __device__ __noinline__ bool warp_pick(const uint32_t* hist, uint32_t need, uint
   }
   const uint32_t excl = incl - slice;
   const uint32_t who = __ballot_sync(0xffffffffu, (excl < need) && (need <= incl));
-  digit = 0;
-  above = 0;
-  if (!who) return false;
+  if (!who) return make_uint3(0u, 0u, 0u);
   const int src = __ffs(who) - 1;
   const uint32_t base = __shfl_sync(0xffffffffu, excl, src);
   const int top = kHistBins - src * per;
@@ -100,13 +101,19 @@ __device__ __noinline__ bool warp_pick(const uint32_t* hist, uint32_t need, uint
   const bool hit0 = above0 < need && need <= above0 + c0;
   const bool hit1 = !hit0 && above0 + c0 < need && need <= above0 + pair;
   const uint32_t found = __ballot_sync(0xffffffffu, hit0 || hit1);
-  if (!found) return false;
+  if (!found) return make_uint3(0u, 0u, 0u);
   const int fl = __ffs(found) - 1;
   const uint32_t d = hit0 ? static_cast<uint32_t>(top - 1 - 2 * lane) : static_cast<uint32_t>(top - 2 - 2 * lane);
   const uint32_t ab = hit0 ? above0 : above0 + c0;
-  digit = __shfl_sync(0xffffffffu, d, fl);
-  above = __shfl_sync(0xffffffffu, ab, fl);
-  return true;
+  return make_uint3(__shfl_sync(0xffffffffu, d, fl), __shfl_sync(0xffffffffu, ab, fl), 1u);
+}
+// (the result comes back in registers: reference out-parameters would put the caller's
+// variables in local memory, whose first touch after the scan misses L1)
+__device__ __forceinline__ bool warp_pick(const uint32_t* hist, uint32_t need, uint32_t& digit, uint32_t& above) {
+  const uint3 r = warp_pick_impl(hist, need);
+  digit = r.x;
+  above = r.y;
+  return r.z != 0;
 }
 
 // Leader: pick on the cluster histogram cl_hist, send (digit, count above it) to every
@@ -147,58 +154,18 @@ __device__ __forceinline__ int warp_span(int n, int unit = 32) {
   return ((n + nw - 1) / nw + unit - 1) / unit * unit;
 }
 
-// Leader, after the barrier that publishes every rank's list: warp w of rank r left its
-// keys (in position order) at cand[w*seg .. w*seg + warp_cnt[0][w]) of rank r.  Pull the
-// segments in (rank, warp) order, which is position order, into the compact list
-// cand[list0 ..), finish the selection and write the row.
-__device__ void leader_finish(TopkSmem& sm, uint2* cand, int seg, int list0, int list_cap, uint32_t d0,
-                              uint32_t above0, int K, int32_t* out_idx, float* out_scores) {
-  const uint32_t nrank = cluster_nctarank();
-  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
-  const int nseg = static_cast<int>(nrank) * nw;
-  for (int i = tid; i < nseg; i += nt) {
-    const uint32_t r = static_cast<uint32_t>(i / nw), w = static_cast<uint32_t>(i % nw);
-    const uint32_t c = r == 0 ? sm.warp_cnt[0][w] : dsmem_ld_u32(dsmem_addr(&sm.warp_cnt[0][w], r));
-    sm.seg_off[i + 1] = c < static_cast<uint32_t>(seg) ? c : static_cast<uint32_t>(seg);
-  }
-  __syncthreads();
-  if (warp == 0) {  // inclusive scan of the segment lengths, 32 segments per step
-    uint32_t carry = 0;
-    for (int b0 = 0; b0 < nseg; b0 += 32) {
-      const int i = b0 + lane;
-      uint32_t v = i < nseg ? sm.seg_off[i + 1] : 0u;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t u = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += u;
-      }
-      if (i < nseg) sm.seg_off[i + 1] = carry + v;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-    if (lane == 0) sm.seg_off[0] = 0;
-  }
-  __syncthreads();
-  // the histogram bounded the total by list_cap; the clamps only guard inconsistent input
-  const uint32_t n = min(sm.seg_off[nseg], static_cast<uint32_t>(list_cap));
-  uint2* list = cand + list0;
-  for (int i = warp; i < nseg; i += nw) {
-    const uint32_t r = static_cast<uint32_t>(i / nw), w = static_cast<uint32_t>(i % nw);
-    const uint32_t off = sm.seg_off[i], c = sm.seg_off[i + 1] - off;
-    const uint2* src = cand + w * seg;
-    for (uint32_t e = lane; e < c && off + e < n; e += 32)
-      list[off + e] = r == 0 ? src[e] : dsmem_ld_v2(dsmem_addr(&src[e], r));
-  }
-  __syncthreads();
-  cand = list;
-
-  // second and third digits over the keys in bin d0
+// Leader, after the barrier that publishes the candidates: cand[0..n) holds, in position
+// order, every key whose top digit is d0 (the bin of the K-th key); above0 keys lie above
+// that bin and are already written.  Finish the last two digits over the candidates and
+// write the selected ones after them: keys > T in position order, then the lowest
+// positions with key == T.
+__device__ void leader_finish(TopkSmem& sm, const uint2* cand, uint32_t n, uint32_t d0, uint32_t above0, int K,
+                              int32_t* out_idx, float* out_scores) {
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
   uint32_t need = static_cast<uint32_t>(K) - above0;
   for (int i = tid; i < kHistBins; i += nt) sm.local[i] = 0;
   __syncthreads();
-  for (uint32_t v = tid; v < n; v += nt) {
-    const uint32_t k = cand[v].x;
-    if ((k >> 21) == d0) atomicAdd(&sm.local[(k >> 10) & 2047u], 1u);
-  }
+  for (uint32_t v = tid; v < n; v += nt) atomicAdd(&sm.local[(cand[v].x >> 10) & 2047u], 1u);
   __syncthreads();
   uint32_t d1, a1;
   block_pick(sm, sm.local, need, d1, a1);
@@ -217,7 +184,8 @@ __device__ void leader_finish(TopkSmem& sm, uint2* cand, int seg, int list0, int
   const uint32_t need_eq = need - a2;                     // >= 1
   const uint32_t gt_total = static_cast<uint32_t>(K) - need_eq;
 
-  // one ordered pass over the list: keys > T, then the first need_eq keys == T
+  // one ordered pass over the candidates: keys > T after the above0 ones, then the first
+  // need_eq keys == T
   const int span = warp_span(static_cast<int>(n));
   const int lo = warp * span, hi = min(static_cast<int>(n), lo + span);
   uint32_t cg = 0, ce = 0;
@@ -229,7 +197,7 @@ __device__ void leader_finish(TopkSmem& sm, uint2* cand, int seg, int list0, int
   }
   if (lane == 0) { sm.warp_cnt[0][warp] = cg; sm.warp_cnt[1][warp] = ce; }
   __syncthreads();
-  uint32_t og = 0, oe = 0;
+  uint32_t og = above0, oe = 0;
   for (int w = 0; w < warp; ++w) { og += sm.warp_cnt[0][w]; oe += sm.warp_cnt[1][w]; }
   const uint32_t lt = (1u << lane) - 1u;
   for (int base = lo; base < hi; base += 32) {
@@ -259,7 +227,7 @@ __device__ void leader_finish(TopkSmem& sm, uint2* cand, int seg, int list0, int
 //   hist0         this CTA's histogram of the keys' top digit (bits 31..21); read only
 //   n_sel         number of selectable positions of the row (positions 0..n_sel-1)
 //   cand          cand_cap free (key, position) slots of shared memory, at the same offset
-//                 in every CTA of the cluster
+//                 in every CTA of the cluster (the leader's copy receives the candidates)
 // Writes out_idx[0..K) (and out_scores if non-null).  Must be called by every thread of
 // every CTA of the cluster (it contains cluster barriers).  The caller must pass another
 // cluster barrier before `cand` or the selector's scratch is written again.
@@ -296,47 +264,61 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, const uint3
   cluster_sync();
   uint32_t d0, above0;
   block_pick(sm, sm.hist[0], static_cast<uint32_t>(K), d0, above0);
-  const uint32_t total = above0 + sm.pick[3];  // cluster-wide count of keys with top digit >= d0
   // every thread has read the picks; the copy is refilled only after a later cluster barrier
   for (int i = tid; i < kHistBins; i += nt) sm.hist[0][i] = 0;
 
-  // each warp's segment holds up to `seg` entries (its slice of the chunk); the leader's
-  // compact list follows the segments.  `chunk` is the same in every CTA, so is the choice.
-  const int seg = warp_span(chunk, 128);
-  if (nw * seg + static_cast<int>(total) <= cand_cap) {
-    // ---- list this CTA's keys with top digit >= d0, in position order, one pass ----
-    const int lo = warp * seg, hi = min(len, lo + seg);
-    uint2* mine = cand + warp * seg;
-    uint32_t o = 0;
-    for (int base = lo; base < hi; base += 128) {
-      const int i0 = base + 4 * lane;
-      uint4 kv = make_uint4(0u, 0u, 0u, 0u);
-      if (i0 + 3 < hi) {
-        kv = *reinterpret_cast<const uint4*>(keys + i0);
-      } else {
-        if (i0 < hi) kv.x = keys[i0];
-        if (i0 + 1 < hi) kv.y = keys[i0 + 1];
-        if (i0 + 2 < hi) kv.z = keys[i0 + 2];
-      }
-      const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
-      uint32_t cnt = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) cnt += (kk[e] != 0u && (kk[e] >> 21) >= d0) ? 1u : 0u;
-      uint32_t incl = cnt;
-#pragma unroll
-      for (int of = 1; of < 32; of <<= 1) {
-        const uint32_t u = __shfl_up_sync(0xffffffffu, incl, of);
-        if (lane >= of) incl += u;
-      }
-      uint32_t at = o + incl - cnt;
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (kk[e] != 0u && (kk[e] >> 21) >= d0) mine[at++] = make_uint2(kk[e], static_cast<uint32_t>(c0 + i0 + e));
-      o += __shfl_sync(0xffffffffu, incl, 31);
+  const uint32_t at_total = sm.pick[3];  // cluster-wide count of keys in bin d0
+  if (at_total <= static_cast<uint32_t>(cand_cap)) {
+    // ---- (1) this CTA's keys above bin d0 and in it, counted per warp slice ----
+    const int span = warp_span(len);
+    const int lo = warp * span, hi = min(len, lo + span);
+    uint32_t cg = 0, ce = 0;
+    for (int base = lo; base < hi; base += 32) {
+      const int i = base + lane;
+      const uint32_t k = i < hi ? keys[i] : 0u;
+      const uint32_t dg = k >> 21;
+      cg += __popc(__ballot_sync(0xffffffffu, k != 0u && dg > d0));
+      ce += __popc(__ballot_sync(0xffffffffu, k != 0u && dg == d0));
     }
-    if (lane == 0) sm.warp_cnt[0][warp] = o;
-    cluster_sync();  // every segment and its length is visible to the leader
-    if (rank == 0) leader_finish(sm, cand, seg, nw * seg, cand_cap - nw * seg, d0, above0, K, out_idx, out_scores);
+    if (lane == 0) { sm.warp_cnt[0][warp] = cg; sm.warp_cnt[1][warp] = ce; }
+    __syncthreads();
+    if (tid < static_cast<int>(nrank)) {  // push this rank's totals into every rank's table
+      uint32_t my_gt = 0, my_eq = 0;
+      for (int w = 0; w < nw; ++w) { my_gt += sm.warp_cnt[0][w]; my_eq += sm.warp_cnt[1][w]; }
+      dsmem_st_u32(dsmem_addr(&sm.counts[0][rank], tid), my_gt);
+      dsmem_st_u32(dsmem_addr(&sm.counts[1][rank], tid), my_eq);
+    }
+    cluster_sync();  // every rank's totals are known everywhere
+    uint32_t og = 0, oe = 0;  // this warp's first output slot / candidate slot
+    for (uint32_t r = 0; r < rank; ++r) { og += sm.counts[0][r]; oe += sm.counts[1][r]; }
+    for (int w = 0; w < warp; ++w) { og += sm.warp_cnt[0][w]; oe += sm.warp_cnt[1][w]; }
+    // ---- (2) keys above bin d0 to the output; keys in it to the leader's candidate list,
+    // both in position order (CTA rank order is position order) ----
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int base = lo; base < hi; base += 32) {
+      const int i = base + lane;
+      const uint32_t k = i < hi ? keys[i] : 0u;
+      const uint32_t dg = k >> 21;
+      const bool up = k != 0u && dg > d0, in = k != 0u && dg == d0;
+      const uint32_t bg = __ballot_sync(0xffffffffu, up);
+      const uint32_t be = __ballot_sync(0xffffffffu, in);
+      if (up) {
+        const uint32_t slot = og + __popc(bg & lt);
+        if (slot < static_cast<uint32_t>(K)) {  // guards the row against an inconsistent count
+          out_idx[slot] = c0 + i;
+          if (out_scores) out_scores[slot] = key_score(k);
+        }
+      }
+      if (in) {
+        const uint32_t slot = oe + __popc(be & lt);
+        if (slot < static_cast<uint32_t>(cand_cap))
+          dsmem_st_v2(dsmem_addr(&cand[slot], 0), make_uint2(k, static_cast<uint32_t>(c0 + i)));
+      }
+      og += __popc(bg);
+      oe += __popc(be);
+    }
+    cluster_sync();  // the leader's candidate list is complete
+    if (rank == 0) leader_finish(sm, cand, at_total, d0, above0, K, out_idx, out_scores);
     return;
   }
 
