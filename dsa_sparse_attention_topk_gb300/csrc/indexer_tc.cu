@@ -230,7 +230,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
     tc::mbar_arrive(&bs.pages_ready);
     if (lane < kProd) {
       // lane l issues tiles t = l (mod kProd): one thread alone cannot issue copies fast
-      // enough to keep the HBM busy, and with an even ring each stage keeps one issuer
+      // enough to keep the HBM busy, and with a ring of a multiple of kProd stages each
+      // stage keeps one issuer
       if (lane == 0) tc::prefetch_tmap(&kmap);
       for (int t = lane; t < ntiles; t += kProd) {
         const int s = t % S, it = t / S;
@@ -444,7 +445,9 @@ cudaError_t launch_gh(const IndexerArgs& a, cudaStream_t s, const char** err) {
   while (C < kMaxCluster && make_plan(G, a.h_i, cap_for(C), 4).total > limit) C *= 2;
   while (C < kMaxCluster && static_cast<long long>(n_groups) * C * 2 <= di.n_sm) C *= 2;
   int stages = kMaxStages;
-  while (stages > 2 && make_plan(G, a.h_i, cap_for(C), stages).total > limit) stages -= 2;  // even
+  // a multiple of kProd (and so of the two MMA issuers): every stage keeps one issuer and
+  // one waiter per barrier
+  while (stages > kProd && make_plan(G, a.h_i, cap_for(C), stages).total > limit) stages -= kProd;
   const Plan pl = make_plan(G, a.h_i, cap_for(C), stages);
   if (pl.total > limit) {
     *err = "indexer: max_ctx too large for the on-chip score buffer";
