@@ -91,6 +91,8 @@ struct Ctl {
 };
 
 constexpr uint32_t kOffQ = 0;
+constexpr int kStagePitch = kVDim * 2 + 16;    // staged bf16 output row (padded against bank conflicts)
+static_assert(128 * kStagePitch <= kQBytes, "the output rows are staged in the Q buffer");
 constexpr uint32_t kOffKv = kQBytes;
 constexpr uint32_t kOffP = kOffKv + 2 * kKvBytes;
 constexpr uint32_t kOffCtl = kOffP + kPBytes;
@@ -333,44 +335,7 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     s_fin[128 + m] = l;
     s_fin[256 + m] = lx;
     asm volatile("bar.sync 1, 256;" ::: "memory");  // S -> P and tail warps
-    // ---- columns 0..447 (TMEM), normalised, as bf16: to the output (one split) or to
-    // the workspace (several splits; merged by sfa_combine_kernel) ----
-    const bool row_ok = m < a.h_s;
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    const size_t slot = (static_cast<size_t>(t) * pl.nsplit + split) * a.h_s + m;
-    __nv_bfloat16* dst = pl.nsplit == 1
-                             ? static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(t) * a.h_s + m) * kVDim
-                             : pl.ws_o + slot * kVDim;
-    for (int c = 0; c < kVLeft; c += 16) {
-      uint32_t r[16];
-      if (nt > 0) {
-        tc::tmem_ld16(tmem + lane_base + c, r);
-        tc::tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] = 0u;
-      }
-      if (row_ok) {
-        uint4 v0 = make_uint4(pack_bf16(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv),
-                              pack_bf16(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv),
-                              pack_bf16(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv),
-                              pack_bf16(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv));
-        uint4 v1 = make_uint4(pack_bf16(__uint_as_float(r[8]) * inv, __uint_as_float(r[9]) * inv),
-                              pack_bf16(__uint_as_float(r[10]) * inv, __uint_as_float(r[11]) * inv),
-                              pack_bf16(__uint_as_float(r[12]) * inv, __uint_as_float(r[13]) * inv),
-                              pack_bf16(__uint_as_float(r[14]) * inv, __uint_as_float(r[15]) * inv));
-        *reinterpret_cast<uint4*>(dst + c) = v0;
-        *reinterpret_cast<uint4*>(dst + c + 8) = v1;
-      }
-    }
-    if (row_ok) {
-      if (pl.nsplit == 1) {
-        if (a.out_lse)
-          a.out_lse[static_cast<size_t>(t) * a.h_s + m] = lx > 0.f ? (m_ref + log2f(lx)) * 0.6931471805599453f : -INFINITY;
-      } else {
-        *reinterpret_cast<float4*>(pl.ws_ml + 4 * slot) = make_float4(m_ref, l, lx, 0.f);
-      }
-    }
+    // (the TMEM columns are written by every warp after the role loops; see below)
   } else if (warp >= kWarpTail0 && warp < kWarpTail0 + 4) {
     // ---------------- tail rounds (warps 8..11): output columns 448..511 ----------------
     const int quarter = warp & 3;
@@ -408,18 +373,15 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     asm volatile("bar.sync 1, 256;" ::: "memory");  // (max, sums) from the S -> P warps
     const float* s_fin = reinterpret_cast<const float*>(s_p);
     const float m_ref = s_fin[m], l = s_fin[128 + m], lx = s_fin[256 + m];
-    const bool row_ok = m < a.h_s;
-    if (row_ok) {
+    // columns 448..511 into the staged output rows (written out below by every warp)
+    {
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* dst = pl.nsplit == 1
-                               ? static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(t) * a.h_s + m) * kVDim
-                               : pl.ws_o + ((static_cast<size_t>(t) * pl.nsplit + split) * a.h_s + m) * kVDim;
+      uint8_t* row = smem + kOffQ + m * kStagePitch + 2 * kVLeft;
 #pragma unroll
-      for (int c = 0; c < kVTail; c += 8) {
-        *reinterpret_cast<uint4*>(dst + kVLeft + c) =
+      for (int c = 0; c < kVTail; c += 8)
+        *reinterpret_cast<uint4*>(row + 2 * c) =
             make_uint4(pack_bf16(ot[c] * inv, ot[c + 1] * inv), pack_bf16(ot[c + 2] * inv, ot[c + 3] * inv),
                        pack_bf16(ot[c + 4] * inv, ot[c + 5] * inv), pack_bf16(ot[c + 6] * inv, ot[c + 7] * inv));
-      }
     }
     (void)m_ref;
     (void)lx;
@@ -547,6 +509,67 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
       tc::fence_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&ctl.kv_full[b]);
+    }
+  }
+  // ---- the output rows, normalised, as bf16: to the output (one split) or to the
+  // workspace (several splits; merged by sfa_combine_kernel).  Columns 0..447 come from
+  // TMEM: warp w reads its lane quadrant (w mod 4), columns 112 (w / 4) .. +112, and stages
+  // them in the (idle) Q buffer next to the tail warps' columns; then every warp writes
+  // whole rows, 512 contiguous bytes per instruction. ----
+  tc::fence_before_sync();
+  __syncthreads();  // the S -> P warps have seen the last product complete and published (m, l, lx)
+  tc::fence_after_sync();
+  {
+    const float* s_fin = reinterpret_cast<const float*>(s_p);  // [3][128]: max, l, lx
+    const int quarter = warp & 3;
+    const int m = quarter * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const float l = s_fin[128 + m];
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    uint8_t* row = smem + kOffQ + m * kStagePitch;
+    const int cbeg = 112 * (warp >> 2);
+    for (int c = cbeg; c < cbeg + 112; c += 32) {
+      uint32_t r[32];
+      const int nc = min(32, cbeg + 112 - c);  // 32, 32, 32, 16
+      if (nt > 0) {
+        tc::tmem_ld16(tmem + lane_base + c, reinterpret_cast<uint32_t(&)[16]>(r[0]));
+        if (nc > 16) tc::tmem_ld16(tmem + lane_base + c + 16, reinterpret_cast<uint32_t(&)[16]>(r[16]));
+        tc::tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; i += 8) {
+        if (i < nc)
+          *reinterpret_cast<uint4*>(row + 2 * (c + i)) =
+              make_uint4(pack_bf16(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv),
+                         pack_bf16(__uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv),
+                         pack_bf16(__uint_as_float(r[i + 4]) * inv, __uint_as_float(r[i + 5]) * inv),
+                         pack_bf16(__uint_as_float(r[i + 6]) * inv, __uint_as_float(r[i + 7]) * inv));
+      }
+    }
+    if (m < a.h_s && warp >= kWarpSoft0 && warp < kWarpSoft0 + 4) {
+      const float m_ref = s_fin[m], lx = s_fin[256 + m];
+      const size_t slot = (static_cast<size_t>(t) * pl.nsplit + split) * a.h_s + m;
+      if (pl.nsplit == 1) {
+        if (a.out_lse)
+          a.out_lse[static_cast<size_t>(t) * a.h_s + m] = lx > 0.f ? (m_ref + log2f(lx)) * 0.6931471805599453f : -INFINITY;
+      } else {
+        *reinterpret_cast<float4*>(pl.ws_ml + 4 * slot) = make_float4(m_ref, l, lx, 0.f);
+      }
+    }
+  }
+  __syncthreads();  // every staged row is complete
+  {
+    // row h: 64 pieces of 16 bytes; thread i takes piece i % 64 of rows i / 64, + 8, ..
+    const int piece = tid & 63;
+    for (int h = tid >> 6; h < a.h_s; h += kThreads / 64) {
+      __nv_bfloat16* dst = pl.nsplit == 1
+                               ? static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(t) * a.h_s + h) * kVDim
+                               : pl.ws_o + ((static_cast<size_t>(t) * pl.nsplit + split) * a.h_s + h) * kVDim;
+      *reinterpret_cast<uint4*>(dst + 8 * piece) =
+          *reinterpret_cast<const uint4*>(smem + kOffQ + h * kStagePitch + 16 * piece);
     }
   }
   tc::fence_before_sync();
