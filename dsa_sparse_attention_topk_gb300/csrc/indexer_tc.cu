@@ -196,6 +196,16 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
     }
     tc::mbar_fence_init();
   }
+  if (warp == 0 && lane >= 1 && lane <= 16) {
+    // warm L2 with the sequence's page-table row (one 128-byte line per lane) while lane 0
+    // reads the sequence information, so the producer's page lookups skip a DRAM access
+    const int sq = a.q_seq[row0];
+    if (sq >= 0 && sq < a.n_seq) {
+      const int32_t* prow = a.page_table + static_cast<size_t>(sq) * a.max_pages;
+      const int i = 32 * (lane - 1);
+      if (i < a.max_pages) asm volatile("prefetch.global.L2 [%0];" :: "l"(prow + i));
+    }
+  }
   if (warp == 1) tc::tmem_alloc(&bs.tmem_base, pl.tmem_cols);
   tc::fence_before_sync();
   __syncthreads();  // barriers, sequence info and the TMEM base are visible to every warp
