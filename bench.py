@@ -174,19 +174,10 @@ def run_ours(args, rank, world, local_rank):
     ws = torch.empty(ws_n, dtype=torch.uint8, device=dev) if ws_n else None
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-    side = torch.cuda.Stream(dev)
-
     def step(inner=False):
-        # the latent-cache writer runs on a second stream beside the indexer-cache writer, as
-        # DsaDecodeLayer.step does; the main stream joins it before the indexer so that the
-        # indexer and SFA follow each other directly (programmatic dependent launch)
-        main = torch.cuda.current_stream(dev)
-        ev[4].record(main)
-        side.wait_event(ev[4])
-        dsa.quant_kv_fp8(d["kv_new"], d["s_new"], layer.kv_cache, stream=side)
-        ev[5].record(side)
+        # the four launches of a decode step on one stream, as DsaDecodeLayer.step issues them
         dsa.quant_kv_mxfp8(d["k_new"], d["s_new"], layer.k_cache)
-        main.wait_event(ev[5])
+        dsa.quant_kv_fp8(d["kv_new"], d["s_new"], layer.kv_cache)
         if inner:
             ev[1].record()
         dsa.indexer_topk(d["q_idx"], d["w"], layer.k_cache, d["page_table"], d["seq_lens"], d["q_seq"],
@@ -197,14 +188,13 @@ def run_ours(args, rank, world, local_rank):
                         wl.sm_scale, out=out, out_lse=lse, workspace=ws)
 
     launches_per_step = 4 + (1 if ws_n else 0)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)] + [torch.cuda.Event() for _ in range(2)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     for _ in range(max(3, args.warmup)):
         flush.zero_()
         ev[0].record(); step(); ev[3].record()
     torch.cuda.synchronize()
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] + [torch.cuda.Event() for _ in range(2)]
-           for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     clocks = ClockSampler(torch.cuda.current_device())
     if world > 1:
         torch.distributed.barrier()

@@ -15,16 +15,18 @@
 // entries, for all heads at once (M = 128 rows of the MMAs; rows >= h_s are zero).
 // Sixteen warps, each role in its own warps so that no role's latency sits in another's
 // loop:
-//   warp 0      every Q K^T: Q (bf16, 128 x 576, resident, loaded once by TMA) times a
-//               gathered tile (32 entries x 576) into one of two S buffers in TMEM, so the
-//               next tile's QK^T runs while the softmax works on this one.
-//   warp 1      every P V: O[:, 0:448] into its TMEM accumulator, and O[:, 448:512] in two
-//               32-column rounds through the tile's S buffer (free once its S was read).
+//   warps 0, 1  Q K^T of the even and the odd tiles: Q (bf16, 128 x 576, resident, loaded
+//               once by TMA) times a gathered tile (32 entries x 576) into one of two S
+//               buffers in TMEM, so the next tile's QK^T runs while the softmax works on this
+//               one.  Two issuing warps, because a single thread issues an MMA only every
+//               ~55 cycles while the operand reads of one take ~40.
 //   warps 4-7   S -> P, one head per thread: online softmax in the exp2 domain with a
 //               lazily updated running max (the accumulator is rescaled only when the max
 //               grows by more than 2^8), P written to shared memory as bf16.
 //   warps 8-11  the tail rounds, added into register accumulators (rescaled with the max
-//               that the S -> P warps publish per tile).
+//               that the S -> P warps publish per tile).  Lane 0 of warp 8 issues every
+//               P V: O[:, 0:448] into its TMEM accumulator, and O[:, 448:512] in two
+//               32-column rounds through the tile's S buffer (free once its S was read).
 //   warps 2, 3, 12-15  gather: index -> page -> record, 16-byte loads of E4M3 codes,
 //               multiply by the tile scale, bf16 into the 128-byte-swizzled operand tile
 //               (double buffered; the next tile's codes are loaded and converted in
@@ -53,10 +55,9 @@ namespace dsa {
 namespace {
 
 constexpr int kTok = 32;                       // selected entries per tile
-constexpr int kWarpQK = 0;                     // issues every Q K^T (and the Q load)
-constexpr int kWarpPV = 1;                     // issues every P V
+constexpr int kWarpQK = 0;                     // warps 0, 1: Q K^T of the even / odd tiles (0: the Q load)
 constexpr int kWarpSoft0 = 4;                  // warps 4..7: S -> P, one TMEM lane quadrant each
-constexpr int kWarpTail0 = 8;                  // warps 8..11: tail rounds, one quadrant each
+constexpr int kWarpTail0 = 8;                  // warps 8..11: tail rounds, one quadrant each; warp 8 issues P V
 constexpr int kGatherWarps = 6;                // warps 2, 3 and 12..15
 constexpr int kThreads = 512;
 constexpr int kQBlock = 128 * 128;             // one 64-column K-block of Q: 128 rows x 128 B
@@ -82,7 +83,7 @@ struct Ctl {
   uint64_t s_free[2];      // S buffer b is free again (its tail rounds have been read)
   uint64_t p_full;         // P of the tile is in shared memory
   uint64_t p_free;         // every P V product of the tile has completed
-  uint64_t m_ready;        // the tile's running max is in the ring
+  uint64_t m_ready[2];     // the running max of the tile in S buffer b is in s_m[b]
   uint64_t tail_full[2];   // a tail round is in S buffer b (two phases per tile)
   uint64_t tail_empty;     // the first tail round has been read
   uint32_t tmem_base;
@@ -156,7 +157,8 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     }
     tc::mbar_init(&ctl.p_full, 4);
     tc::mbar_init(&ctl.p_free, 1);
-    tc::mbar_init(&ctl.m_ready, 4);
+    tc::mbar_init(&ctl.m_ready[0], 4);
+    tc::mbar_init(&ctl.m_ready[1], 4);
     tc::mbar_init(&ctl.tail_empty, 4);
     tc::mbar_fence_init();
   }
@@ -176,83 +178,40 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
   const int32_t* idx = a.idx + static_cast<size_t>(t) * a.topk;
   if (tid == 0 && !seq_ok && split == 0) flag(a.status, DSA_STATUS_BAD_SEQ);
 
-  if (warp == kWarpQK || warp == kWarpPV) {
-    // ---------------- MMA issuers ----------------
+  if (warp == kWarpQK || warp == kWarpQK + 1) {
+    // ---------------- Q K^T issuers ----------------
+    // warp kWarpQK + b issues the tiles j = b (mod 2), from lane 0: one thread issues an MMA
+    // only every ~55 cycles and two lanes of one warp take turns, while two warps keep the
+    // tensor core's operand reads busy.  Each warp owns one S buffer and one KV buffer, so
+    // every barrier it waits on keeps a single waiter and its operands stay fixed.
+    const int b = warp - kWarpQK;
     if (lane == 0) {
-      if (warp == kWarpQK) {
+      if (b == 0) {
         tc::prefetch_tmap(&qmap);
         tc::mbar_arrive_expect_tx(&ctl.q_full, kQBytes);
         for (int kb = 0; kb < 9; ++kb) tc::tma_load_3d(s_q + kb * kQBlock, &qmap, kb * 64, 0, t, &ctl.q_full);
       }
-    }
-    if (warp == kWarpQK && lane < 2) {
-      // lane l issues the tiles j = l (mod 2): one thread alone issues an MMA only every
-      // ~55-80 cycles, two keep the tensor core's operand reads busy.  Each lane owns one
-      // S buffer and one KV buffer, so every barrier it waits on keeps a single waiter.
-      {
-        const uint32_t id_qk = tc::idesc_bf16(kTok, false, false);
-        tc::mbar_wait(&ctl.q_full, 0, abort, a.status);
-        // descriptors advance by adding (byte offset >> 4) to the start-address field
-        const uint64_t qd0 = tc::desc_kmajor_sw128(smem_u32(s_q));
-        const uint64_t kd0 = tc::desc_kmajor_sw128(smem_u32(s_kv));
-        for (int j = lane; j < nt; j += 2) {
-          // S = Q K^T of tile j into S buffer j & 1
-          const int b = j & 1;
-          tc::mbar_wait(&ctl.kv_full[b], (j >> 1) & 1, abort, a.status);
-          tc::mbar_wait(&ctl.s_free[b], ((j >> 1) & 1) ^ 1, abort, a.status);
-          tc::fence_after_sync();
-          const uint64_t kd = kd0 + static_cast<uint64_t>(b * (kKvBytes >> 4));
-          const uint32_t d = tmem + kColS + kTok * b;
+      const uint32_t id_qk = tc::idesc_bf16(kTok, false, false);
+      tc::mbar_wait(&ctl.q_full, 0, abort, a.status);
+      // descriptors advance by adding (byte offset >> 4) to the start-address field
+      const uint64_t qd0 = tc::desc_kmajor_sw128(smem_u32(s_q));
+      const uint64_t kd = tc::desc_kmajor_sw128(smem_u32(s_kv + b * kKvBytes));
+      const uint32_t d = tmem + kColS + kTok * b;
+      for (int j = b; j < nt; j += 2) {
+        // S = Q K^T of tile j into S buffer b
+        tc::mbar_wait(&ctl.kv_full[b], (j >> 1) & 1, abort, a.status);
+        tc::mbar_wait(&ctl.s_free[b], ((j >> 1) & 1) ^ 1, abort, a.status);
+        tc::fence_after_sync();
 #pragma unroll
-          for (int st = 0; st < 36; ++st) {
-            const uint32_t kb = st >> 2, k = st & 3;
-            tc::mma_bf16(d, qd0 + (kb * (kQBlock >> 4) + 2 * k), kd + (kb * (kKvBlock >> 4) + 2 * k), id_qk, st > 0);
-          }
-          tc::commit(&ctl.s_full[b]);
-          tc::commit(&ctl.kv_empty[b]);
+        for (int st = 0; st < 36; ++st) {
+          const uint32_t kb = st >> 2, k = st & 3;
+          tc::mma_bf16(d, qd0 + (kb * (kQBlock >> 4) + 2 * k), kd + (kb * (kKvBlock >> 4) + 2 * k), id_qk, st > 0);
         }
+        tc::commit(&ctl.s_full[b]);
+        tc::commit(&ctl.kv_empty[b]);
       }
     }
-    if (warp == kWarpPV && lane == 0) {
-      {
-        const uint32_t id_v0 = tc::idesc_bf16(256, false, true);
-        const uint32_t id_v1 = tc::idesc_bf16(192, false, true);
-        const uint32_t id_vt = tc::idesc_bf16(kTok, false, true);
-        for (int j = 0; j < nt; ++j) {
-          // O += P V of tile j; the last 64 output columns go through S buffer j & 1 in two
-          // rounds of 32 that the tail warps add into registers
-          const int b = j & 1;
-          uint8_t* kv = s_kv + b * kKvBytes;
-          tc::mbar_wait(&ctl.kv_full[b], (j >> 1) & 1, abort, a.status);
-          tc::mbar_wait(&ctl.p_full, j & 1, abort, a.status);
-          tc::fence_after_sync();
-          uint64_t pd[2], vd[2];
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            pd[ks] = tc::smem_desc(smem_u32(s_p + ks * 256), 128, 512, 0);
-            vd[ks] = tc::smem_desc(smem_u32(kv + ks * 2048), kKvBlock, 1024, 2);  // 16 entries = two 8-row groups
-          }
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            tc::mma_bf16(tmem + 0, pd[ks], vd[ks], id_v0, j > 0 || ks > 0);
-            tc::mma_bf16(tmem + 256, pd[ks], vd[ks] + 4 * (kKvBlock >> 4), id_v1, j > 0 || ks > 0);
-          }
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            if (r == 1) {
-              tc::mbar_wait(&ctl.tail_empty, j & 1, abort, a.status);
-              tc::fence_after_sync();
-            }
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks)  // columns 448 + 32 r .. : 64 r bytes into the swizzle atom
-              tc::mma_bf16(tmem + kColS + kTok * b, pd[ks], vd[ks] + (7 * (kKvBlock >> 4) + 4 * r), id_vt, ks > 0);
-            tc::commit(&ctl.tail_full[b]);
-          }
-          tc::commit(&ctl.kv_empty[b]);
-          tc::commit(&ctl.p_free);
-        }
-      }
-    }
+    __syncwarp();
   } else if (warp >= kWarpSoft0 && warp < kWarpSoft0 + 4) {
     // ---------------- S -> P (warps 4..7) ----------------
     const int quarter = warp & 3;
@@ -285,7 +244,20 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
       // the tail warps rescale their part of the accumulator with the same max
       s_m[b * 128 + m] = m_new;
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&ctl.m_ready);
+      if (lane == 0) tc::mbar_arrive(&ctl.m_ready[b]);
+      // the weights need only the new max: they are formed while the previous tile's
+      // products may still be running
+      uint32_t pk[16];
+      float lsum = 0.f, lxsum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const float p0 = (m_new == -INFINITY) ? 0.f : fast_exp2(x[i] - m_new);
+        const float p1 = (m_new == -INFINITY) ? 0.f : fast_exp2(x[i + 1] - m_new);
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+        lsum += __low2float(pb) + __high2float(pb);
+        lxsum += p0 + p1;
+        pk[i >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
+      }
       // every P V product of the previous tile has completed: P may be overwritten and the
       // TMEM accumulator rescaled
       if (j > 0) tc::mbar_wait(&ctl.p_free, (j - 1) & 1, abort, a.status);
@@ -301,22 +273,9 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
         }
         tc::tmem_wait_st();
       }
-      l *= alpha;
-      lx *= alpha;
+      l = l * alpha + lsum;
+      lx = lx * alpha + lxsum;
       m_ref = m_new;
-      uint32_t pk[16];
-      float lsum = 0.f, lxsum = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const float p0 = (m_ref == -INFINITY) ? 0.f : fast_exp2(x[i] - m_ref);
-        const float p1 = (m_ref == -INFINITY) ? 0.f : fast_exp2(x[i + 1] - m_ref);
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-        lsum += __low2float(pb) + __high2float(pb);
-        lxsum += p0 + p1;
-        pk[i >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
-      }
-      l += lsum;
-      lx += lxsum;
       // P row m: core matrix (m/8, chunk c) at (m/8)*512 + c*128, row offset (m%8)*16
       uint8_t* prow = s_p + (m >> 3) * 512 + (m & 7) * 16;
 #pragma unroll
@@ -337,18 +296,45 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     asm volatile("bar.sync 1, 256;" ::: "memory");  // S -> P and tail warps
     // (the TMEM columns are written by every warp after the role loops; see below)
   } else if (warp >= kWarpTail0 && warp < kWarpTail0 + 4) {
-    // ---------------- tail rounds (warps 8..11): output columns 448..511 ----------------
+    // ---- P V issue (warp 8, lane 0) and the tail rounds (warps 8..11): output columns 448..511 ----
     const int quarter = warp & 3;
     const int m = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const bool pv = warp == kWarpTail0 && lane == 0;
+    const uint32_t id_v0 = tc::idesc_bf16(256, false, true);
+    const uint32_t id_v1 = tc::idesc_bf16(192, false, true);
+    const uint32_t id_vt = tc::idesc_bf16(kTok, false, true);
     float m_prev = -INFINITY;
     float ot[kVTail];
 #pragma unroll
     for (int i = 0; i < kVTail; ++i) ot[i] = 0.f;
     for (int j = 0; j < nt; ++j) {
       const int b = j & 1;
+      uint64_t pd[2], vd[2];
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        pd[ks] = tc::smem_desc(smem_u32(s_p + ks * 256), 128, 512, 0);
+        vd[ks] = tc::smem_desc(smem_u32(s_kv + b * kKvBytes + ks * 2048), kKvBlock, 1024, 2);  // 16 entries = two 8-row groups
+      }
+      if (pv) {
+        // O += P V of tile j: columns 0..447 into the TMEM accumulator, 448..511 through S
+        // buffer b (its S has been read) in two rounds of 32 that the tail warps add up
+        tc::mbar_wait(&ctl.kv_full[b], (j >> 1) & 1, abort, a.status);
+        tc::mbar_wait(&ctl.p_full, j & 1, abort, a.status);
+        tc::fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+          tc::mma_bf16(tmem + 0, pd[ks], vd[ks], id_v0, j > 0 || ks > 0);
+          tc::mma_bf16(tmem + 256, pd[ks], vd[ks] + 4 * (kKvBlock >> 4), id_v1, j > 0 || ks > 0);
+        }
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)  // columns 448.. : 7 K-blocks into the tile
+          tc::mma_bf16(tmem + kColS + kTok * b, pd[ks], vd[ks] + 7 * (kKvBlock >> 4), id_vt, ks > 0);
+        tc::commit(&ctl.tail_full[b]);
+      }
+      __syncwarp();
       // the running max the S -> P warps used for this tile: rescale by the same factor
-      tc::mbar_wait(&ctl.m_ready, j & 1, abort, a.status);
+      tc::mbar_wait(&ctl.m_ready[b], (j >> 1) & 1, abort, a.status);
       const float m_new = s_m[b * 128 + m];
       const float alpha = (m_new == m_prev) ? 1.f : fast_exp2(m_prev - m_new);  // 2^-inf = 0
       m_prev = m_new;
@@ -358,6 +344,20 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
       }
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
+        if (r == 1) {
+          if (pv) {
+            // the first round has been read by every tail warp: the second replaces it
+            tc::mbar_wait(&ctl.tail_empty, j & 1, abort, a.status);
+            tc::fence_after_sync();
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks)  // columns 480.. : 64 bytes further into the swizzle atom
+              tc::mma_bf16(tmem + kColS + kTok * b, pd[ks], vd[ks] + (7 * (kKvBlock >> 4) + 4), id_vt, ks > 0);
+            tc::commit(&ctl.tail_full[b]);
+            tc::commit(&ctl.kv_empty[b]);
+            tc::commit(&ctl.p_free);
+          }
+          __syncwarp();
+        }
         tc::mbar_wait(&ctl.tail_full[b], r, abort, a.status);
         tc::fence_after_sync();
         uint32_t rr[32];
@@ -493,6 +493,10 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
         }
         o0s[k] = make_uint4(o[0], o[1], o[2], o[3]);
         o1s[k] = make_uint4(o[4], o[5], o[6], o[7]);
+        // pin the converted words here: left to itself the compiler moves the conversion
+        // behind the wait below, where it delays the tile by its whole length
+        asm volatile("" : "+r"(o0s[k].x), "+r"(o0s[k].y), "+r"(o0s[k].z), "+r"(o0s[k].w),
+                          "+r"(o1s[k].x), "+r"(o1s[k].y), "+r"(o1s[k].z), "+r"(o1s[k].w));
       }
       load_codes(p1, pg1);
       p1 = p2; pg1 = pg2; p2 = p3; pg2 = pg3n; p3 = p4n;

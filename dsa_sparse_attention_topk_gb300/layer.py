@@ -24,7 +24,6 @@ class DsaDecodeLayer:
         self.kv_cache = alloc_kv_cache(num_pages, self.device)
         self._ws = {}
         self._bufs = {}
-        self._side = None  # stream for the latent-cache writer of a step
 
     def write(self, k, kv, slot_mapping):
         """Quantise and store new tokens: k bf16 [n, 128], kv bf16 [n, 576], slots int64 [n]."""
@@ -61,24 +60,14 @@ class DsaDecodeLayer:
              max_ctx, q_group=1):
         """Write this step's tokens, then decode.
 
-        The latent-cache writer runs on a second stream beside the indexer-cache writer; the
-        current stream joins it before the indexer, so that the indexer and sparse attention
-        follow each other directly (the library launches with programmatic dependent launch).
+        All four launches go on the current stream, one after the other: the library launches
+        with programmatic dependent launch, so each kernel's launch and set-up overlap the end
+        of the one before.  (A second stream for the latent-cache writer measured slower: the
+        cross-stream join costs more than the writer.)
         """
         main = torch.cuda.current_stream(self.device)
-        if self._side is None:
-            self._side = torch.cuda.Stream(self.device)
-        side = self._side
-        ready = torch.cuda.Event()
-        ready.record(main)
-        side.wait_event(ready)
-        quant_kv_fp8(kv_new, slots_new, self.kv_cache, stream=side)
-        kv_new.record_stream(side)
-        slots_new.record_stream(side)
-        written = torch.cuda.Event()
-        written.record(side)
         quant_kv_mxfp8(k_new, slots_new, self.k_cache, stream=main)
-        main.wait_event(written)
+        quant_kv_fp8(kv_new, slots_new, self.kv_cache, stream=main)
         n_q = q_idx.shape[0]
         b = self._buffers(n_q)
         indexer_topk(q_idx, w, self.k_cache, page_table, seq_lens, q_seq, q_pos, self.topk, max_ctx,
