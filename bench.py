@@ -175,9 +175,8 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def step(inner=False):
-        # the four launches of a decode step on one stream, as DsaDecodeLayer.step issues them
-        dsa.quant_kv_mxfp8(d["k_new"], d["s_new"], layer.k_cache)
-        dsa.quant_kv_fp8(d["kv_new"], d["s_new"], layer.kv_cache)
+        # the launches of a decode step on one stream, as DsaDecodeLayer.step issues them
+        dsa.quant_kv(d["k_new"], d["kv_new"], d["s_new"], layer.k_cache, layer.kv_cache)
         if inner:
             ev[1].record()
         dsa.indexer_topk(d["q_idx"], d["w"], layer.k_cache, d["page_table"], d["seq_lens"], d["q_seq"],
@@ -187,7 +186,7 @@ def run_ours(args, rank, world, local_rank):
         dsa.sparse_attn(d["q_sfa"], layer.kv_cache, d["page_table"], d["seq_lens"], d["q_seq"], idx,
                         wl.sm_scale, out=out, out_lse=lse, workspace=ws)
 
-    launches_per_step = 4 + (1 if ws_n else 0)
+    launches_per_step = 3 + (1 if ws_n else 0)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     for _ in range(max(3, args.warmup)):
         flush.zero_()

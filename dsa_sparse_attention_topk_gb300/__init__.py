@@ -9,6 +9,7 @@ Functions (same names as the C entry points, without the ``dsa_`` prefix):
 
 * ``quant_kv_mxfp8(k, slot_mapping, k_cache)``  -- cache writer, MXFP8 indexer keys
 * ``quant_kv_fp8(kv, slot_mapping, kv_cache)``   -- cache writer, FP8 MLA latent rows
+* ``quant_kv(k, kv, slot_mapping, k_cache, kv_cache)`` -- both writers in one launch
 * ``indexer_topk(...)``                          -- fused Lightning Indexer + Top-K
 * ``indexer_scores(...)``                        -- the same scores written in full
 * ``sparse_attn(...)``                           -- Sparse Flash Attention
@@ -54,6 +55,7 @@ _SZ = ctypes.c_size_t
 _SIGS = {
     "dsa_quant_kv_mxfp8": (ctypes.c_int, [_P, _P, _I32, _P, _I64, _P]),
     "dsa_quant_kv_fp8": (ctypes.c_int, [_P, _P, _I32, _P, _I64, _P]),
+    "dsa_quant_kv": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _I64, _P]),
     "dsa_indexer_topk": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _I64, _P, _I32, _P, _P, _P,
                                         _I32, _I32, _I32, _P, _P, _P]),
     "dsa_indexer_scores": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _I64, _P, _I32, _P, _P, _P,
@@ -134,6 +136,20 @@ def quant_kv_fp8(kv, slot_mapping, kv_cache, stream=None):
     num_slots = kv_cache.numel() // (PAGE_SIZE * KVCACHE_TOKEN_BYTES) * PAGE_SIZE
     _check(lib().dsa_quant_kv_fp8(_ptr(kv), _ptr(slot_mapping), kv.shape[0], _ptr(kv_cache),
                                   num_slots, _stream(stream)))
+
+
+def quant_kv(k, kv, slot_mapping, k_cache, kv_cache, stream=None):
+    """Both cache writers in one launch: k bf16 [n, 128] -> k_cache, kv bf16 [n, 576] ->
+    kv_cache, at the same int64 slots [n]."""
+    _need(k, torch.bfloat16, "k")
+    _need(kv, torch.bfloat16, "kv")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    if k.shape[0] != kv.shape[0] or k.shape[0] != slot_mapping.shape[0]:
+        raise ValueError("quant_kv: k, kv and slot_mapping must have the same number of tokens")
+    num_slots = min(k_cache.numel() // KCACHE_PAGE_BYTES,
+                    kv_cache.numel() // (PAGE_SIZE * KVCACHE_TOKEN_BYTES)) * PAGE_SIZE
+    _check(lib().dsa_quant_kv(_ptr(k), _ptr(kv), _ptr(slot_mapping), k.shape[0], _ptr(k_cache), _ptr(kv_cache),
+                              num_slots, _stream(stream)))
 
 
 def indexer_topk(q, w, k_cache, page_table, seq_lens, q_seq, q_pos, topk, max_ctx,

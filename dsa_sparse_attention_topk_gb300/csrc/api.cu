@@ -88,6 +88,24 @@ int dsa_quant_kv_fp8(const void* kv_bf16, const int64_t* slot_mapping, int32_t n
   return e == cudaSuccess ? DSA_OK : cuda_fail(e, "quant_kv_fp8 launch");
 }
 
+int dsa_quant_kv(const void* k_bf16, const void* kv_bf16, const int64_t* slot_mapping, int32_t n_tokens,
+                 uint8_t* k_cache, uint8_t* kv_cache, int64_t num_slots, void* stream) {
+  if (n_tokens < 0) return fail(DSA_ERR_INVALID_ARG, "quant_kv: n_tokens < 0");
+  if (n_tokens == 0) return DSA_OK;
+  if (!k_bf16 || !kv_bf16 || !slot_mapping || !k_cache || !kv_cache)
+    return fail(DSA_ERR_INVALID_ARG, "quant_kv: null pointer");
+  if (!aligned(k_bf16, 16) || !aligned(kv_bf16, 16) || !aligned(k_cache, 16) || !aligned(kv_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return fail(DSA_ERR_INVALID_ARG, "quant_kv: rows and caches must be 16-byte aligned");
+  if (num_slots <= 0 || num_slots % DSA_PAGE_SIZE)
+    return fail(DSA_ERR_INVALID_ARG, "quant_kv: num_slots must be a positive multiple of 64");
+  unsigned* st = status_ptr();
+  if (!st) return fail(DSA_ERR_CUDA, "quant_kv: no CUDA device");
+  cudaError_t e = dsa::launch_quant_both(k_bf16, kv_bf16, slot_mapping, n_tokens, k_cache, kv_cache, num_slots, st,
+                                         static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSA_OK : cuda_fail(e, "quant_kv launch");
+}
+
 static int check_indexer(const char* who, const void* q_bf16, const float* w, int32_t n_q, int32_t h_i,
                          int32_t q_group, const uint8_t* k_cache, int64_t num_pages,
                          const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,

@@ -80,6 +80,8 @@ cudaError_t launch_quant_mxfp8(const void* k, const int64_t* slots, int n_tokens
                                int64_t num_slots, unsigned* status, cudaStream_t s);
 cudaError_t launch_quant_fp8(const void* kv, const int64_t* slots, int n_tokens, uint8_t* cache,
                              int64_t num_slots, unsigned* status, cudaStream_t s);
+cudaError_t launch_quant_both(const void* k, const void* kv, const int64_t* slots, int n_tokens, uint8_t* k_cache,
+                              uint8_t* kv_cache, int64_t num_slots, unsigned* status, cudaStream_t s);
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s, const char** err);
 cudaError_t launch_sfa(const SfaArgs& a, cudaStream_t s, const char** err);
 size_t sfa_workspace_bytes(int n_q, int h_s, int topk);

@@ -270,6 +270,15 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
     constexpr int kPrepWarps = kThreads / 32 - 1;
     constexpr int kBatch = 8;
     const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(a.q);
+    // the head weights are requested first, so that their loads share the round trip of the
+    // query rows' loads below
+    constexpr int kWPer = (Np + kThreads - 33) / (kThreads - 32);
+    float wv[kWPer];
+#pragma unroll
+    for (int r = 0; r < kWPer; ++r) {
+      const int i = tid - 32 + r * (kThreads - 32), j = i / Hp, h = i % Hp;
+      wv[r] = (i < G * Hp && h < H) ? a.w[static_cast<size_t>(row0 + j) * H + h] : 0.f;
+    }
     for (int n0 = warp - 1; n0 < Np; n0 += kPrepWarps * kBatch) {
       uint2 raw[kBatch];
 #pragma unroll
@@ -297,9 +306,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
     // scale words of padding rows up to the end of the last 128-row block
     for (int n = Np + tid - 32; n < ((Np + 127) / 128) * 128; n += kThreads - 32)
       s_sfb[(n >> 7) * 128 + (n & 31) * 4 + ((n >> 5) & 3)] = 0x7F7F7F7Fu;
-    for (int i = tid - 32; i < G * Hp; i += kThreads - 32) {
-      const int j = i / Hp, h = i % Hp;
-      s_w[i] = h < H ? a.w[static_cast<size_t>(row0 + j) * H + h] : 0.f;
+#pragma unroll
+    for (int r = 0; r < kWPer; ++r) {
+      const int i = tid - 32 + r * (kThreads - 32);
+      if (i < G * Hp) s_w[i] = wv[r];
     }
     tc::fence_async_smem();
     asm volatile("bar.sync 1, %0;" :: "r"(kThreads - 32) : "memory");  // every warp but the producer

@@ -6,7 +6,7 @@
 // cache follows section "FP8 KVCache with Per-Token-Head-Tile Quantization for SFA"
 // (one fp32 scale per 128-element tile of each token).
 //
-// Both kernels give one warp to one token: the reads are 8-byte (k) or 8/4-byte (kv)
+// Every writer gives one warp to one token: the reads are 8-byte (k) or 8/4-byte (kv)
 // coalesced loads, the amax reductions are warp shuffles, and the writes land in the
 // token's cache row.  They are HBM-bound elementwise kernels (a few bytes of math per
 // byte moved) and run once per new token, outside the decode hot loop.
@@ -19,43 +19,44 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;
 
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-quant_mxfp8_kernel(const __nv_bfloat16* __restrict__ k, const int64_t* __restrict__ slots,
-                   int n_tokens, uint8_t* __restrict__ cache, int64_t num_slots,
-                   unsigned* status) {
-  pdl_launch_dependents();
-  pdl_wait();
+// One warp writes token t's indexer key: 128 values, four MXFP8 groups of 32 (group =
+// lane / 8, four values per lane).  The loads are issued first (load_k_token), so that a
+// caller writing both caches can have every load of a token in flight at once.
+struct KTok {
+  uint2 raw;     // this lane's four values (dims 4 lane ..)
+  int64_t slot;
+};
+__device__ __forceinline__ KTok load_k_token(const __nv_bfloat16* __restrict__ k, const int64_t* __restrict__ slots,
+                                             int64_t t) {
   const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp; t < n_tokens;
-       t += static_cast<int64_t>(gridDim.x) * kWarpsPerBlock) {
-    // the token's values and its slot are requested together (one memory round trip)
-    const uint2 raw = *reinterpret_cast<const uint2*>(k + t * kIdxDim + 4 * lane);  // dims 4 lane ..
-    const int64_t slot = slots[t];
-    if (slot < 0) continue;
-    if (slot >= num_slots) {
-      if (lane == 0) flag(status, DSA_STATUS_BAD_PAGE);
-      continue;
-    }
-    // group = lane / 8
-    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-    float x[4] = {__low2float(a), __high2float(a), __low2float(b), __high2float(b)};
-    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const int e = mx_shared_exp(amax);
-    const float inv = exp2i(-e);  // exact power of two: x * inv is exact
-    uint32_t codes = 0;
-    if (amax > 0.f) {
-      codes = static_cast<uint32_t>(f32x2_to_e4m3x2(x[0] * inv, x[1] * inv)) |
-              (static_cast<uint32_t>(f32x2_to_e4m3x2(x[2] * inv, x[3] * inv)) << 16);
-    }
-    uint8_t* page = cache + (slot / kPage) * kKPageBytes;
-    const int row = static_cast<int>(slot % kPage);
-    *reinterpret_cast<uint32_t*>(page + row * kIdxDim + 4 * lane) = codes;
-    if ((lane & 7) == 0) page[kKScaleOff + row * 4 + (lane >> 3)] = static_cast<uint8_t>(e + 127);
+  return KTok{*reinterpret_cast<const uint2*>(k + t * kIdxDim + 4 * lane), slots[t]};
+}
+__device__ __forceinline__ void store_k_token(const KTok& in, uint8_t* __restrict__ cache, int64_t num_slots,
+                                              unsigned* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t slot = in.slot;
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (lane == 0) flag(status, DSA_STATUS_BAD_PAGE);
+    return;
   }
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&in.raw.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&in.raw.y);
+  float x[4] = {__low2float(a), __high2float(a), __low2float(b), __high2float(b)};
+  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const int e = mx_shared_exp(amax);
+  const float inv = exp2i(-e);  // exact power of two: x * inv is exact
+  uint32_t codes = 0;
+  if (amax > 0.f) {
+    codes = static_cast<uint32_t>(f32x2_to_e4m3x2(x[0] * inv, x[1] * inv)) |
+            (static_cast<uint32_t>(f32x2_to_e4m3x2(x[2] * inv, x[3] * inv)) << 16);
+  }
+  uint8_t* page = cache + (slot / kPage) * kKPageBytes;
+  const int row = static_cast<int>(slot % kPage);
+  *reinterpret_cast<uint32_t*>(page + row * kIdxDim + 4 * lane) = codes;
+  if ((lane & 7) == 0) page[kKScaleOff + row * 4 + (lane >> 3)] = static_cast<uint8_t>(e + 127);
 }
 
 // |x| / s rounded to the nearest float and then nudged to "round to odd" when inexact:
@@ -72,68 +73,110 @@ __device__ __forceinline__ float quotient_round_to_odd(float x, float s) {
   return copysignf(__uint_as_float(qb), x);
 }
 
+// One warp writes token t's latent row: four 128-wide tiles (four values per lane) and the
+// 64-wide rope tile (two per lane), each with its fp32 scale; loads first, as above.
+struct KvTok {
+  uint2 raws[4];           // this lane's four values of each full tile
+  __nv_bfloat162 rope;     // this lane's two rope values
+  int64_t slot;
+};
+__device__ __forceinline__ KvTok load_kv_token(const __nv_bfloat16* __restrict__ kv, const int64_t* __restrict__ slots,
+                                               int64_t t) {
+  const int lane = threadIdx.x & 31;
+  const __nv_bfloat16* src = kv + t * kLatent;
+  KvTok in;
+#pragma unroll
+  for (int tile = 0; tile < 4; ++tile) in.raws[tile] = *reinterpret_cast<const uint2*>(src + tile * 128 + 4 * lane);
+  in.rope = *reinterpret_cast<const __nv_bfloat162*>(src + 512 + 2 * lane);
+  in.slot = slots[t];
+  return in;
+}
+__device__ __forceinline__ void store_kv_token(const KvTok& in, uint8_t* __restrict__ cache, int64_t num_slots,
+                                               unsigned* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t slot = in.slot;
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (lane == 0) flag(status, DSA_STATUS_BAD_PAGE);
+    return;
+  }
+  uint8_t* rec = cache + slot * kKvTokBytes;
+  float scales[kKvTiles];
+#pragma unroll
+  for (int tile = 0; tile < 4; ++tile) {  // four full 128-wide tiles: 4 elements per lane
+    const uint2 raw = in.raws[tile];
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+    float x[4] = {__low2float(a), __high2float(a), __low2float(b), __high2float(b)};
+    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = __fdiv_rn(amax, 448.0f);
+    uint32_t codes = 0;
+    if (s > 0.f) {
+      codes = static_cast<uint32_t>(f32x2_to_e4m3x2(quotient_round_to_odd(x[0], s),
+                                                    quotient_round_to_odd(x[1], s))) |
+              (static_cast<uint32_t>(f32x2_to_e4m3x2(quotient_round_to_odd(x[2], s),
+                                                     quotient_round_to_odd(x[3], s))) << 16);
+    }
+    *reinterpret_cast<uint32_t*>(rec + tile * 128 + 4 * lane) = codes;
+    scales[tile] = s;
+  }
+  {  // the 64-wide rope tile: 2 elements per lane
+    float x0 = __low2float(in.rope), x1 = __high2float(in.rope);
+    float amax = fmaxf(fabsf(x0), fabsf(x1));
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = __fdiv_rn(amax, 448.0f);
+    uint16_t codes = 0;
+    if (s > 0.f) codes = f32x2_to_e4m3x2(quotient_round_to_odd(x0, s), quotient_round_to_odd(x1, s));
+    *reinterpret_cast<uint16_t*>(rec + 512 + 2 * lane) = codes;
+    scales[4] = s;
+  }
+  if (lane == 0) {
+    *reinterpret_cast<uint4*>(rec + kKvScaleOff) =
+        make_uint4(__float_as_uint(scales[0]), __float_as_uint(scales[1]),
+                   __float_as_uint(scales[2]), __float_as_uint(scales[3]));
+  } else if (lane == 1) {
+    *reinterpret_cast<uint4*>(rec + kKvScaleOff + 16) = make_uint4(__float_as_uint(scales[4]), 0u, 0u, 0u);
+  }
+}
+
+// Token loop shared by the writers: warp w of block b takes tokens b * 8 + w, + the grid.
+#define DSA_FOR_TOKENS(t)                                                                                    \
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5); t < n_tokens;   \
+       t += static_cast<int64_t>(gridDim.x) * kWarpsPerBlock)
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+quant_mxfp8_kernel(const __nv_bfloat16* __restrict__ k, const int64_t* __restrict__ slots,
+                   int n_tokens, uint8_t* __restrict__ cache, int64_t num_slots,
+                   unsigned* status) {
+  pdl_launch_dependents();
+  pdl_wait();
+  DSA_FOR_TOKENS(t) store_k_token(load_k_token(k, slots, t), cache, num_slots, status);
+}
+
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 quant_fp8_kernel(const __nv_bfloat16* __restrict__ kv, const int64_t* __restrict__ slots,
                  int n_tokens, uint8_t* __restrict__ cache, int64_t num_slots,
                  unsigned* status) {
   pdl_launch_dependents();
   pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp; t < n_tokens;
-       t += static_cast<int64_t>(gridDim.x) * kWarpsPerBlock) {
-    // every value of the token and its slot are requested together (one memory round trip)
-    const __nv_bfloat16* src = kv + t * kLatent;
-    uint2 raws[4];
-#pragma unroll
-    for (int tile = 0; tile < 4; ++tile) raws[tile] = *reinterpret_cast<const uint2*>(src + tile * 128 + 4 * lane);
-    const __nv_bfloat162 rope = *reinterpret_cast<const __nv_bfloat162*>(src + 512 + 2 * lane);
-    const int64_t slot = slots[t];
-    if (slot < 0) continue;
-    if (slot >= num_slots) {
-      if (lane == 0) flag(status, DSA_STATUS_BAD_PAGE);
-      continue;
-    }
-    uint8_t* rec = cache + slot * kKvTokBytes;
-    float scales[kKvTiles];
-#pragma unroll
-    for (int tile = 0; tile < 4; ++tile) {  // four full 128-wide tiles: 4 elements per lane
-      const uint2 raw = raws[tile];
-      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-      float x[4] = {__low2float(a), __high2float(a), __low2float(b), __high2float(b)};
-      float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float s = __fdiv_rn(amax, 448.0f);
-      uint32_t codes = 0;
-      if (s > 0.f) {
-        codes = static_cast<uint32_t>(f32x2_to_e4m3x2(quotient_round_to_odd(x[0], s),
-                                                      quotient_round_to_odd(x[1], s))) |
-                (static_cast<uint32_t>(f32x2_to_e4m3x2(quotient_round_to_odd(x[2], s),
-                                                       quotient_round_to_odd(x[3], s))) << 16);
-      }
-      *reinterpret_cast<uint32_t*>(rec + tile * 128 + 4 * lane) = codes;
-      scales[tile] = s;
-    }
-    {  // the 64-wide rope tile: 2 elements per lane
-      float x0 = __low2float(rope), x1 = __high2float(rope);
-      float amax = fmaxf(fabsf(x0), fabsf(x1));
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float s = __fdiv_rn(amax, 448.0f);
-      uint16_t codes = 0;
-      if (s > 0.f) codes = f32x2_to_e4m3x2(quotient_round_to_odd(x0, s), quotient_round_to_odd(x1, s));
-      *reinterpret_cast<uint16_t*>(rec + 512 + 2 * lane) = codes;
-      scales[4] = s;
-    }
-    if (lane == 0) {
-      *reinterpret_cast<uint4*>(rec + kKvScaleOff) =
-          make_uint4(__float_as_uint(scales[0]), __float_as_uint(scales[1]),
-                     __float_as_uint(scales[2]), __float_as_uint(scales[3]));
-    } else if (lane == 1) {
-      *reinterpret_cast<uint4*>(rec + kKvScaleOff + 16) = make_uint4(__float_as_uint(scales[4]), 0u, 0u, 0u);
-    }
+  DSA_FOR_TOKENS(t) store_kv_token(load_kv_token(kv, slots, t), cache, num_slots, status);
+}
+
+// Both caches of a token in one launch (a decode step writes both before its indexer).
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+quant_both_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ kv,
+                  const int64_t* __restrict__ slots, int n_tokens, uint8_t* __restrict__ k_cache,
+                  uint8_t* __restrict__ kv_cache, int64_t num_slots, unsigned* status) {
+  pdl_launch_dependents();
+  pdl_wait();
+  DSA_FOR_TOKENS(t) {
+    const KTok kin = load_k_token(k, slots, t);
+    const KvTok kvin = load_kv_token(kv, slots, t);
+    store_k_token(kin, k_cache, num_slots, status);
+    store_kv_token(kvin, kv_cache, num_slots, status);
   }
 }
 
@@ -156,6 +199,14 @@ cudaError_t launch_quant_fp8(const void* kv, const int64_t* slots, int n_tokens,
   if (n_tokens == 0) return cudaSuccess;
   return launch_pdl(quant_fp8_kernel, dim3(grid_for(n_tokens)), dim3(kWarpsPerBlock * 32), 0, s, 1,
                     static_cast<const __nv_bfloat16*>(kv), slots, n_tokens, cache, num_slots, status);
+}
+
+cudaError_t launch_quant_both(const void* k, const void* kv, const int64_t* slots, int n_tokens, uint8_t* k_cache,
+                              uint8_t* kv_cache, int64_t num_slots, unsigned* status, cudaStream_t s) {
+  if (n_tokens == 0) return cudaSuccess;
+  return launch_pdl(quant_both_kernel, dim3(grid_for(n_tokens)), dim3(kWarpsPerBlock * 32), 0, s, 1,
+                    static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(kv), slots, n_tokens,
+                    k_cache, kv_cache, num_slots, status);
 }
 
 }  // namespace dsa

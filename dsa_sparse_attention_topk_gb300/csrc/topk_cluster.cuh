@@ -255,13 +255,18 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, const uint3
     return;
   }
 
-  // ---- first digit: add this CTA's histogram into every CTA's copy, pick locally ----
-  for (int i = tid; i < kHistBins; i += nt) {
-    const uint32_t c = hist0[i];
-    if (c)
-      for (uint32_t r = 0; r < nrank; ++r) dsmem_add_u32(dsmem_addr(&sm.hist[0][i], r), c);
+  // ---- first digit: every CTA sums all ranks' histograms (final since the caller's
+  // cluster barrier, and never written again) into its own copy and picks locally ----
+  for (int i = 4 * tid; i < kHistBins; i += 4 * nt) {
+    uint4 sum = *reinterpret_cast<const uint4*>(hist0 + i);
+    for (uint32_t r = 0; r < nrank; ++r) {
+      if (r == rank) continue;
+      const uint4 v = dsmem_ld_v4(dsmem_addr(hist0 + i, r));
+      sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+    }
+    *reinterpret_cast<uint4*>(&sm.hist[0][i]) = sum;
   }
-  cluster_sync();
+  __syncthreads();
   uint32_t d0, above0;
   block_pick(sm, sm.hist[0], static_cast<uint32_t>(K), d0, above0);
   // every thread has read the picks; the copy is refilled only after a later cluster barrier

@@ -5,7 +5,7 @@ computation is a call into the C ABI.
 
 import torch
 
-from . import (alloc_k_cache, alloc_kv_cache, quant_kv_mxfp8, quant_kv_fp8, indexer_topk,
+from . import (alloc_k_cache, alloc_kv_cache, quant_kv_mxfp8, quant_kv_fp8, quant_kv, indexer_topk,
                sparse_attn, sparse_attn_workspace_size)
 
 
@@ -58,16 +58,14 @@ class DsaDecodeLayer:
 
     def step(self, k_new, kv_new, slots_new, q_idx, w, q_sfa, page_table, seq_lens, q_seq, q_pos,
              max_ctx, q_group=1):
-        """Write this step's tokens, then decode.
+        """Write this step's tokens (both caches, one launch), then decode.
 
-        All four launches go on the current stream, one after the other: the library launches
-        with programmatic dependent launch, so each kernel's launch and set-up overlap the end
-        of the one before.  (A second stream for the latent-cache writer measured slower: the
-        cross-stream join costs more than the writer.)
+        The three launches go on the current stream, one after the other: the library
+        launches with programmatic dependent launch, so each kernel's launch and set-up
+        overlap the end of the one before.
         """
         main = torch.cuda.current_stream(self.device)
-        quant_kv_mxfp8(k_new, slots_new, self.k_cache, stream=main)
-        quant_kv_fp8(kv_new, slots_new, self.kv_cache, stream=main)
+        quant_kv(k_new, kv_new, slots_new, self.k_cache, self.kv_cache, stream=main)
         n_q = q_idx.shape[0]
         b = self._buffers(n_q)
         indexer_topk(q_idx, w, self.k_cache, page_table, seq_lens, q_seq, q_pos, self.topk, max_ctx,

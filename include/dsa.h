@@ -9,7 +9,8 @@
  *      (dsa_indexer_topk);
  *   2. Sparse Flash Attention that gathers the selected entries of a paged FP8 MLA
  *      latent cache and runs online-softmax attention over them (dsa_sparse_attn).
- * Two cache writers fill the caches (dsa_quant_kv_mxfp8, dsa_quant_kv_fp8).
+ * Two cache writers fill the caches (dsa_quant_kv_mxfp8, dsa_quant_kv_fp8; dsa_quant_kv
+ * runs both in one launch).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -102,6 +103,20 @@ int dsa_quant_kv_mxfp8(const void* k_bf16, const int64_t* slot_mapping, int32_t 
  */
 int dsa_quant_kv_fp8(const void* kv_bf16, const int64_t* slot_mapping, int32_t n_tokens,
                      uint8_t* kv_cache, int64_t num_slots, void* stream);
+
+/*
+ * dsa_quant_kv -- both writers above for the same tokens in one launch: token i's key
+ * k_bf16[i] goes to the MXFP8 K-cache and its latent row kv_bf16[i] to the FP8 KV-cache,
+ * both at slot_mapping[i] (the two caches share one page table).  The codes and scales are
+ * exactly those of dsa_quant_kv_mxfp8 followed by dsa_quant_kv_fp8; a decode step uses it
+ * to write its new tokens with one kernel before the indexer.  The pages give the two
+ * formats, not this pairing.
+ *   k_bf16, kv_bf16, slot_mapping   as for the two writers above (same n_tokens).
+ *   k_cache, kv_cache               both hold at least num_slots slots.
+ * Errors and skipped slots as for the two writers.
+ */
+int dsa_quant_kv(const void* k_bf16, const void* kv_bf16, const int64_t* slot_mapping, int32_t n_tokens,
+                 uint8_t* k_cache, uint8_t* kv_cache, int64_t num_slots, void* stream);
 
 /*
  * dsa_indexer_topk -- fused Lightning Indexer + Top-K over the paged MXFP8 K-cache.

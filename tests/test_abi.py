@@ -86,6 +86,11 @@ def test_quant_and_sfa_reject_bad_arguments(dsa):
     assert lib.dsa_quant_kv_fp8(None, P(16), 4, P(16), 64, None) == -1
     assert lib.dsa_quant_kv_fp8(P(8), P(16), 4, P(16), 64, None) == -1        # misaligned source
     assert lib.dsa_quant_kv_mxfp8(P(16), P(16), 0, P(16), 64, None) == 0      # nothing to do
+    assert lib.dsa_quant_kv(P(16), P(16), P(16), 4, P(16), P(16), 100, None) == -1   # not a page multiple
+    assert lib.dsa_quant_kv(P(16), None, P(16), 4, P(16), P(16), 64, None) == -1     # no latent rows
+    assert lib.dsa_quant_kv(P(16), P(16), P(16), 4, P(16), P(24), 64, None) == -1    # misaligned cache
+    assert lib.dsa_quant_kv(P(16), P(16), P(16), -1, P(16), P(16), 64, None) == -1
+    assert lib.dsa_quant_kv(None, None, None, 0, None, None, 64, None) == 0          # nothing to do
     args = [P(16), 1, 128, P(16), 1, P(16), 1, P(16), P(16), 1, P(16), 2048, ctypes.c_float(0.07),
             P(16), None, None, 0, None]
     bad_h = list(args); bad_h[2] = 129

@@ -104,3 +104,33 @@ def test_negative_slots_skip_and_out_of_range_slots_flag(dsa):
     assert np.array_equal(page[:128], c_ref[1])      # token 1 -> slot 0
     assert np.all(page[128:8192] == 0xAB)             # nothing else written
     assert dsa.device_status() == 0                   # cleared by the read
+
+
+def test_paired_writer_matches_the_oracle_and_skips_like_the_single_writers(dsa):
+    # dsa_quant_kv writes both caches in one launch: the same codes and scales as the two
+    # writers, checked against the oracle, with a skipped (-1) and an out-of-range slot
+    n = 64
+    k = _special_rows(128, n, 4)
+    kv = _special_rows(576, n, 5)
+    slots = torch.arange(n, dtype=torch.int64)
+    slots[7] = -1
+    slots[9] = 64  # past a one-page cache: skipped and flagged
+    kc = dsa.alloc_k_cache(1)
+    vc = dsa.alloc_kv_cache(1)
+    kc.fill_(0xAB)
+    vc.fill_(0xAB)
+    dsa.quant_kv(k.cuda(), kv.cuda(), slots.cuda(), kc, vc)
+    assert dsa.device_status() & 1, "slot 64 of a one-page cache must flag BAD_PAGE"
+    written = np.array([i for i in range(n) if i not in (7, 9)])
+    page = kc.cpu().numpy()
+    c_ref, s_ref = oracle.mxfp8_quantize(k.double().numpy())
+    assert np.array_equal(page[:8192].reshape(64, 128)[written], c_ref[written])
+    assert np.array_equal(page[8192:].reshape(64, 4)[written], s_ref[written])
+    assert np.all(page[:8192].reshape(64, 128)[[7, 9]] == 0xAB)
+    vc_ref, vs_ref = oracle.fp8_tile_quantize(kv.double().numpy())
+    codes, scales, _ = _kvcache_rows(vc, written)
+    assert np.array_equal(codes, vc_ref[written])
+    assert np.array_equal(scales.view(np.uint32), vs_ref[written].view(np.uint32))
+    untouched, _, _ = _kvcache_rows(vc, np.array([7, 9]))
+    assert np.all(untouched == 0xAB)
+    assert dsa.device_status() == 0
