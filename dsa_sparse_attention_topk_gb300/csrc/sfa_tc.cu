@@ -24,9 +24,11 @@
 //               lazily updated running max (the accumulator is rescaled only when the max
 //               grows by more than 2^8), P written to shared memory as bf16.
 //   warps 8-11  the tail rounds, added into register accumulators (rescaled with the max
-//               that the S -> P warps publish per tile).  Lane 0 of warp 8 issues every
-//               P V: O[:, 0:448] into its TMEM accumulator, and O[:, 448:512] in two
-//               32-column rounds through the tile's S buffer (free once its S was read).
+//               that the S -> P warps publish per tile).
+//   lane 0 of warp 4 also issues every P V once the tile's P is stored: O[:, 0:448] into
+//               its TMEM accumulator, and O[:, 448:512] in two 32-column rounds through the
+//               tile's S buffer (free once its S was read), the second at the start of the
+//               next tile, so that neither the tail warps nor the softmax wait for the issue.
 //   warps 2, 3, 12-15  gather: index -> page -> record, 16-byte loads of E4M3 codes,
 //               multiply by the tile scale, bf16 into the 128-byte-swizzled operand tile
 //               (double buffered; the next tile's codes are loaded and converted in
@@ -56,8 +58,8 @@ namespace {
 
 constexpr int kTok = 32;                       // selected entries per tile
 constexpr int kWarpQK = 0;                     // warps 0, 1: Q K^T of the even / odd tiles (0: the Q load)
-constexpr int kWarpSoft0 = 4;                  // warps 4..7: S -> P, one TMEM lane quadrant each
-constexpr int kWarpTail0 = 8;                  // warps 8..11: tail rounds, one quadrant each; warp 8 issues P V
+constexpr int kWarpSoft0 = 4;                  // warps 4..7: S -> P, one TMEM lane quadrant each; warp 4 issues P V
+constexpr int kWarpTail0 = 8;                  // warps 8..11: tail rounds, one quadrant each
 constexpr int kGatherWarps = 6;                // warps 2, 3 and 12..15
 constexpr int kThreads = 512;
 constexpr int kQBlock = 128 * 128;             // one 64-column K-block of Q: 128 rows x 128 B
@@ -178,6 +180,52 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
   const int32_t* idx = a.idx + static_cast<size_t>(t) * a.topk;
   if (tid == 0 && !seq_ok && split == 0) flag(a.status, DSA_STATUS_BAD_SEQ);
 
+  // P V of tile j, issued by one thread: O[:, 0:448] into the TMEM accumulator, and
+  // O[:, 448:512] in two 32-column rounds through S buffer j & 1 (its S has been read) that
+  // the tail warps add into registers.  The second round waits until the tail warps have
+  // read the first, so its issue is deferred to the start of the next tile (pv_second_round),
+  // and the issuing thread goes on with the softmax meanwhile.
+  const uint32_t id_v0 = tc::idesc_bf16(256, false, true);
+  const uint32_t id_v1 = tc::idesc_bf16(192, false, true);
+  const uint32_t id_vt = tc::idesc_bf16(kTok, false, true);
+  auto pv_desc = [&](int j, int ks, uint64_t& pd, uint64_t& vd) {
+    pd = tc::smem_desc(smem_u32(s_p + ks * 256), 128, 512, 0);
+    vd = tc::smem_desc(smem_u32(s_kv + (j & 1) * kKvBytes + ks * 2048), kKvBlock, 1024, 2);  // 16 entries = two 8-row groups
+  };
+  auto pv_main = [&](int j) {
+    const int b = j & 1;
+    tc::mbar_wait(&ctl.p_full, j & 1, abort, a.status);  // every S -> P warp has stored its rows
+    tc::fence_after_sync();
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      uint64_t pd, vd;
+      pv_desc(j, ks, pd, vd);
+      tc::mma_bf16(tmem + 0, pd, vd, id_v0, j > 0 || ks > 0);
+      tc::mma_bf16(tmem + 256, pd, vd + 4 * (kKvBlock >> 4), id_v1, j > 0 || ks > 0);
+    }
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {  // columns 448.. : 7 K-blocks into the tile
+      uint64_t pd, vd;
+      pv_desc(j, ks, pd, vd);
+      tc::mma_bf16(tmem + kColS + kTok * b, pd, vd + 7 * (kKvBlock >> 4), id_vt, ks > 0);
+    }
+    tc::commit(&ctl.tail_full[b]);
+  };
+  auto pv_second_round = [&](int j) {
+    const int b = j & 1;
+    tc::mbar_wait(&ctl.tail_empty, j & 1, abort, a.status);  // every tail warp has read round one
+    tc::fence_after_sync();
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {  // columns 480.. : 64 bytes further into the swizzle atom
+      uint64_t pd, vd;
+      pv_desc(j, ks, pd, vd);
+      tc::mma_bf16(tmem + kColS + kTok * b, pd, vd + (7 * (kKvBlock >> 4) + 4), id_vt, ks > 0);
+    }
+    tc::commit(&ctl.tail_full[b]);
+    tc::commit(&ctl.kv_empty[b]);
+    tc::commit(&ctl.p_free);
+  };
+
   if (warp == kWarpQK || warp == kWarpQK + 1) {
     // ---------------- Q K^T issuers ----------------
     // warp kWarpQK + b issues the tiles j = b (mod 2), from lane 0: one thread issues an MMA
@@ -221,8 +269,12 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     // l sums the bf16-rounded weights that the P V product uses (it normalises O);
     // lx sums the unrounded weights (it gives the log-sum-exp)
     float m_ref = -INFINITY, l = 0.f, lx = 0.f;
+    // lane 0 of warp 4 issues every P V (see pv_main, pv_second_round)
+    const bool pv = warp == kWarpSoft0 && lane == 0;
     for (int j = 0; j < nt; ++j) {
       const int b = j & 1;
+      if (pv && j > 0) pv_second_round(j - 1);
+      __syncwarp();
       // the gather warps flag the tile's real entries before they release the buffer
       tc::mbar_wait(&ctl.kv_full[b], (j >> 1) & 1, abort, a.status);
       const uint32_t mask = __ballot_sync(0xffffffffu, ctl.valid[b][lane] != 0);
@@ -285,7 +337,11 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&ctl.p_full);
+      if (pv) pv_main(j);
+      __syncwarp();
     }
+    if (pv && nt > 0) pv_second_round(nt - 1);
+    __syncwarp();
     // every product has completed; hand (max, sums) to the tail warps through the P buffer
     if (nt > 0) tc::mbar_wait(&ctl.p_free, (nt - 1) & 1, abort, a.status);
     tc::fence_after_sync();
@@ -296,43 +352,16 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     asm volatile("bar.sync 1, 256;" ::: "memory");  // S -> P and tail warps
     // (the TMEM columns are written by every warp after the role loops; see below)
   } else if (warp >= kWarpTail0 && warp < kWarpTail0 + 4) {
-    // ---- P V issue (warp 8, lane 0) and the tail rounds (warps 8..11): output columns 448..511 ----
+    // ---------------- tail rounds (warps 8..11): output columns 448..511 ----------------
     const int quarter = warp & 3;
     const int m = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const bool pv = warp == kWarpTail0 && lane == 0;
-    const uint32_t id_v0 = tc::idesc_bf16(256, false, true);
-    const uint32_t id_v1 = tc::idesc_bf16(192, false, true);
-    const uint32_t id_vt = tc::idesc_bf16(kTok, false, true);
     float m_prev = -INFINITY;
     float ot[kVTail];
 #pragma unroll
     for (int i = 0; i < kVTail; ++i) ot[i] = 0.f;
     for (int j = 0; j < nt; ++j) {
       const int b = j & 1;
-      uint64_t pd[2], vd[2];
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {
-        pd[ks] = tc::smem_desc(smem_u32(s_p + ks * 256), 128, 512, 0);
-        vd[ks] = tc::smem_desc(smem_u32(s_kv + b * kKvBytes + ks * 2048), kKvBlock, 1024, 2);  // 16 entries = two 8-row groups
-      }
-      if (pv) {
-        // O += P V of tile j: columns 0..447 into the TMEM accumulator, 448..511 through S
-        // buffer b (its S has been read) in two rounds of 32 that the tail warps add up
-        tc::mbar_wait(&ctl.kv_full[b], (j >> 1) & 1, abort, a.status);
-        tc::mbar_wait(&ctl.p_full, j & 1, abort, a.status);
-        tc::fence_after_sync();
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          tc::mma_bf16(tmem + 0, pd[ks], vd[ks], id_v0, j > 0 || ks > 0);
-          tc::mma_bf16(tmem + 256, pd[ks], vd[ks] + 4 * (kKvBlock >> 4), id_v1, j > 0 || ks > 0);
-        }
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks)  // columns 448.. : 7 K-blocks into the tile
-          tc::mma_bf16(tmem + kColS + kTok * b, pd[ks], vd[ks] + 7 * (kKvBlock >> 4), id_vt, ks > 0);
-        tc::commit(&ctl.tail_full[b]);
-      }
-      __syncwarp();
       // the running max the S -> P warps used for this tile: rescale by the same factor
       tc::mbar_wait(&ctl.m_ready[b], (j >> 1) & 1, abort, a.status);
       const float m_new = s_m[b * 128 + m];
@@ -344,20 +373,6 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
       }
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        if (r == 1) {
-          if (pv) {
-            // the first round has been read by every tail warp: the second replaces it
-            tc::mbar_wait(&ctl.tail_empty, j & 1, abort, a.status);
-            tc::fence_after_sync();
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks)  // columns 480.. : 64 bytes further into the swizzle atom
-              tc::mma_bf16(tmem + kColS + kTok * b, pd[ks], vd[ks] + (7 * (kKvBlock >> 4) + 4), id_vt, ks > 0);
-            tc::commit(&ctl.tail_full[b]);
-            tc::commit(&ctl.kv_empty[b]);
-            tc::commit(&ctl.p_free);
-          }
-          __syncwarp();
-        }
         tc::mbar_wait(&ctl.tail_full[b], r, abort, a.status);
         tc::fence_after_sync();
         uint32_t rr[32];
