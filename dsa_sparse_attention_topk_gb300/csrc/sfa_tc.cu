@@ -196,13 +196,7 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     const int b = j & 1;
     tc::mbar_wait(&ctl.p_full, j & 1, abort, a.status);  // every S -> P warp has stored its rows
     tc::fence_after_sync();
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-      uint64_t pd, vd;
-      pv_desc(j, ks, pd, vd);
-      tc::mma_bf16(tmem + 0, pd, vd, id_v0, j > 0 || ks > 0);
-      tc::mma_bf16(tmem + 256, pd, vd + 4 * (kKvBlock >> 4), id_v1, j > 0 || ks > 0);
-    }
+    // the first tail round goes first: the tail warps read it while the large products run
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {  // columns 448.. : 7 K-blocks into the tile
       uint64_t pd, vd;
@@ -210,6 +204,13 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
       tc::mma_bf16(tmem + kColS + kTok * b, pd, vd + 7 * (kKvBlock >> 4), id_vt, ks > 0);
     }
     tc::commit(&ctl.tail_full[b]);
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      uint64_t pd, vd;
+      pv_desc(j, ks, pd, vd);
+      tc::mma_bf16(tmem + 0, pd, vd, id_v0, j > 0 || ks > 0);
+      tc::mma_bf16(tmem + 256, pd, vd + 4 * (kKvBlock >> 4), id_v1, j > 0 || ks > 0);
+    }
   };
   auto pv_second_round = [&](int j) {
     const int b = j & 1;
