@@ -27,8 +27,9 @@
 //               that the S -> P warps publish per tile).
 //   lane 0 of warp 4 also issues every P V once the tile's P is stored: O[:, 0:448] into
 //               its TMEM accumulator, and O[:, 448:512] in two 32-column rounds through the
-//               tile's S buffer (free once its S was read), the second at the start of the
-//               next tile, so that neither the tail warps nor the softmax wait for the issue.
+//               tile's S buffer (free once its S was read).  The first round goes ahead of
+//               the large products, so the tail warps read it while those run; the second
+//               is issued at the start of the next tile, so the softmax never waits for it.
 //   warps 2, 3, 12-15  gather: index -> page -> record, 16-byte loads of E4M3 codes,
 //               multiply by the tile scale, bf16 into the 128-byte-swizzled operand tile
 //               (double buffered; the next tile's codes are loaded and converted in
@@ -37,7 +38,9 @@
 // TMEM (512 columns): O[:, 0:448] in columns 0..447, S buffers in 448..479 (even tiles)
 // and 480..511 (odd tiles).  At N = 32 an MMA costs ~40 cycles of the SM's operand reads
 // whatever issues it (a 4 KB Q slice and a 1 KB tile slice from shared memory), so QK^T's
-// 36 K-steps per tile set the pace; everything else is arranged to overlap with them.
+// 36 K-steps are the largest cost of a tile.  With two KV buffers next to the resident Q,
+// a buffer is refilled only after its tile's P V products, so the chain gather -> Q K^T ->
+// softmax -> P V -> tail rounds, once per two tiles, sets the pace (~4400 cycles a tile).
 // Several splits of a row write their partial outputs (each normalised by its own sum,
 // bf16) with their running max and sums to the workspace; a small kernel merges them
 // (log-sum-exp weights).  (Merging inside
