@@ -29,8 +29,8 @@ CASES = {
     "short_ctx": lambda: W.make("short_ctx"),
     "ragged_h100": lambda: W.custom([300, 1, 2500, 129], h_i=16, h_s=100, topk=256, seed=17),
     "mtp_h128": lambda: W.custom([1500, 700], per_seq=2, h_i=16, h_s=128, topk=512, seed=18),
-    # 20 rows -> 7 splits per row, 40 rows -> 3: split counts that do not divide the 512
-    # output columns the cluster's ranks share out
+    # 20 rows -> 7 splits per row, 40 rows -> 3: split counts that do not divide the 64
+    # tiles of a 2048-entry row evenly
     "rows20_split7": lambda: W.custom([300 + 37 * i for i in range(20)], h_i=8, h_s=32, topk=256, seed=19),
     "rows40_split3": lambda: W.custom([200 + 11 * i for i in range(40)], h_i=8, h_s=48, topk=128, seed=20),
 }
@@ -86,7 +86,7 @@ def test_sfa_padding_order_empty_and_bad_index(dsa):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["decode_b32_ctx32k", "long_mtp_b4_ctx128k"])
+@pytest.mark.parametrize("name", ["decode_b32_ctx32k", "long_mtp_b4_ctx128k", "prefill_4k_over_64k"])
 def test_sfa_full_size_sampled(dsa, name):
     wl = W.make(name)
     dw = DeviceWorkload(wl)
