@@ -264,6 +264,7 @@ def run_ours(args, rank, world, local_rank):
     sel = np.minimum(n_max, wl.topk)
     kv_bytes = int(sel.sum()) * KV_BYTES_PER_ENTRY
     sfa_flops = float(sel.sum()) * wl.h_s * (576 + 512) * 2
+    idx_flops = float(groups.sum()) * wl.q_group * wl.h_i * 128 * 2  # q . k over every scanned position
     step_bytes = idx_bytes + kv_bytes
 
     # dominant kernel by time share
@@ -300,6 +301,18 @@ def run_ours(args, rank, world, local_rank):
         "kernels_ms": {"cache_write": round(t_write, 5), "indexer_topk": round(t_idx, 5),
                        "sparse_attn": round(t_sfa, 5)},
         "roofline": roof,
+        # both kernels against their own bounds (the dominant one is "roofline" above): the
+        # indexer against HBM and the FP8 tensor peak (nominally twice bf16's), SFA against
+        # the bf16 tensor peak
+        "kernel_rooflines": {
+            "indexer_topk": {"bound": "hbm", "achieved_gbs": round(idx_bytes / (t_idx * 1e-3) / 1e9, 1),
+                             "frac_hbm": round(idx_bytes / (t_idx * 1e-3) / 1e9 / hbm, 4),
+                             "fp8_tflops": round(idx_flops / (t_idx * 1e-3) / 1e12, 1),
+                             "frac_fp8": round(idx_flops / (t_idx * 1e-3) / 1e12 / (2 * peaks.get("bf16_tflops", 1900.0)), 4)},
+            "sparse_attn": {"bound": "tensor", "bf16_tflops": round(sfa_flops / (t_sfa * 1e-3) / 1e12, 1),
+                            "frac_bf16": round(sfa_flops / (t_sfa * 1e-3) / 1e12 / peaks.get("bf16_tflops", 1900.0), 4),
+                            "achieved_gbs": round(kv_bytes / (t_sfa * 1e-3) / 1e9, 1)},
+        },
         "e2e": {"value": round(n_q * world / t_e2e, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 4)},
         "gpu_launches": K * launches_per_step,
