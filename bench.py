@@ -175,14 +175,19 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def step(inner=False):
-        # the launches of a decode step on one stream, as DsaDecodeLayer.step issues them
+        if not inner:
+            # a decode step as DsaDecodeLayer.step issues it: one library call
+            dsa.decode_step(d["k_new"], d["kv_new"], d["s_new"], layer.k_cache, layer.kv_cache, d["q_idx"],
+                            d["w"], d["q_sfa"], d["page_table"], d["seq_lens"], d["q_seq"], d["q_pos"], wl.topk,
+                            wl.max_ctx, wl.sm_scale, q_group=wl.q_group, out_idx=idx, out=out, out_lse=lse,
+                            workspace=ws)
+            return
+        # the per-kernel breakdown: the same three stages as separate calls, events between
         dsa.quant_kv(d["k_new"], d["kv_new"], d["s_new"], layer.k_cache, layer.kv_cache)
-        if inner:
-            ev[1].record()
+        ev[1].record()
         dsa.indexer_topk(d["q_idx"], d["w"], layer.k_cache, d["page_table"], d["seq_lens"], d["q_seq"],
                          d["q_pos"], wl.topk, wl.max_ctx, q_group=wl.q_group, out_idx=idx)
-        if inner:
-            ev[2].record()
+        ev[2].record()
         dsa.sparse_attn(d["q_sfa"], layer.kv_cache, d["page_table"], d["seq_lens"], d["q_seq"], idx,
                         wl.sm_scale, out=out, out_lse=lse, workspace=ws)
 

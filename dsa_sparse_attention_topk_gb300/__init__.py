@@ -10,6 +10,7 @@ Functions (same names as the C entry points, without the ``dsa_`` prefix):
 * ``quant_kv_mxfp8(k, slot_mapping, k_cache)``  -- cache writer, MXFP8 indexer keys
 * ``quant_kv_fp8(kv, slot_mapping, kv_cache)``   -- cache writer, FP8 MLA latent rows
 * ``quant_kv(k, kv, slot_mapping, k_cache, kv_cache)`` -- both writers in one launch
+* ``decode_step(...)``  -- writers, indexer + Top-K and SFA of one decode step in one call
 * ``indexer_topk(...)``                          -- fused Lightning Indexer + Top-K
 * ``indexer_scores(...)``                        -- the same scores written in full
 * ``sparse_attn(...)``                           -- Sparse Flash Attention
@@ -65,6 +66,9 @@ _SIGS = {
                                        _F32, _P, _P, _P, _SZ, _P]),
     "dsa_sparse_attn_noalloc": (ctypes.c_int, [_P, _I32, _I32, _P, _I64, _P, _I32, _P, _P, _I32, _P, _I32,
                                                _F32, _P, _P, _P]),
+    "dsa_decode_step": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32,
+                                       _P, _P, _I32, _P, _P, _I32, _I32, _P, _P, _I32, _F32, _P, _P, _P, _SZ,
+                                       _P]),
     "dsa_device_status": (ctypes.c_int, [_P]),
     "dsa_last_error": (ctypes.c_char_p, []),
     "dsa_version": (ctypes.c_int, []),
@@ -203,6 +207,38 @@ def sparse_attn(q, kv_cache, page_table, seq_lens, q_seq, topk_idx, sm_scale, ou
                                  _ptr(workspace), 0 if workspace is None else workspace.numel(),
                                  _stream(stream)))
     return out, out_lse
+
+
+def decode_step(k_new, kv_new, slot_mapping, k_cache, kv_cache, q_idx, w, q_sfa, page_table, seq_lens,
+                q_seq, q_pos, topk, max_ctx, sm_scale, q_group=1, out_idx=None, out=None, out_lse=None,
+                workspace=None, stream=None):
+    """One decode step in one call: write k_new / kv_new (bf16 [n_new, 128] / [n_new, 576],
+    int64 slots [n_new]) into the caches, then the fused indexer + Top-K, then Sparse Flash
+    Attention over the selected entries.  Returns (out bf16 [n_q, h_s, 512], out_lse or
+    None, out_idx int32 [n_q, topk])."""
+    _need(k_new, torch.bfloat16, "k_new")
+    _need(kv_new, torch.bfloat16, "kv_new")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    n_new = k_new.shape[0]
+    if kv_new.shape[0] != n_new or slot_mapping.shape[0] != n_new:
+        raise ValueError("decode_step: k_new, kv_new and slot_mapping must have the same number of tokens")
+    n_q, h_i, _ = q_idx.shape
+    h_s = q_sfa.shape[1]
+    if out_idx is None:
+        out_idx = torch.empty(n_q, topk, dtype=torch.int32, device=q_idx.device)
+    if out is None:
+        out = torch.empty(n_q, h_s, V_DIM, dtype=torch.bfloat16, device=q_idx.device)
+    ws_need = sparse_attn_workspace_size(n_q, h_s, topk)
+    if workspace is None and ws_need:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q_idx.device)
+    num_pages = min(k_cache.numel() // KCACHE_PAGE_BYTES, kv_cache.numel() // (PAGE_SIZE * KVCACHE_TOKEN_BYTES))
+    _check(lib().dsa_decode_step(_ptr(k_new), _ptr(kv_new), _ptr(slot_mapping), n_new, _ptr(k_cache),
+                                 _ptr(kv_cache), num_pages, _ptr(page_table), page_table.shape[1],
+                                 _ptr(seq_lens), seq_lens.shape[0], max_ctx, n_q, _ptr(q_seq), _ptr(q_pos),
+                                 q_group, _ptr(q_idx), _ptr(w), h_i, topk, _ptr(out_idx), _ptr(q_sfa), h_s,
+                                 float(sm_scale), _ptr(out), _ptr(out_lse), _ptr(workspace),
+                                 0 if workspace is None else workspace.numel(), _stream(stream)))
+    return out, out_lse, out_idx
 
 
 def sparse_attn_noalloc(q, kv_cache, page_table, seq_lens, q_seq, topk_idx, sm_scale, out=None,

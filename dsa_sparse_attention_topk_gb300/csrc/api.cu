@@ -2,6 +2,7 @@
 // the per-thread error message.  Every compute step runs in the kernels behind
 // dsa_launch.h; nothing here touches tensor data on the host.
 
+#include <cstdint>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -199,6 +200,59 @@ int dsa_sparse_attn(const void* q_bf16, int32_t n_q, int32_t h_s, const uint8_t*
   const char* why = nullptr;
   cudaError_t e = dsa::launch_sfa(a, static_cast<cudaStream_t>(stream), &why);
   if (e != cudaSuccess) return why ? fail(DSA_ERR_UNSUPPORTED, "%s", why) : cuda_fail(e, "sparse_attn launch");
+  return DSA_OK;
+}
+
+int dsa_decode_step(const void* k_new_bf16, const void* kv_new_bf16, const int64_t* slot_mapping, int32_t n_new,
+                    uint8_t* k_cache, uint8_t* kv_cache, int64_t num_pages, const int32_t* page_table,
+                    int32_t max_pages, const int32_t* seq_lens, int32_t n_seq, int32_t max_ctx, int32_t n_q,
+                    const int32_t* q_seq, const int32_t* q_pos, int32_t q_group, const void* q_idx_bf16,
+                    const float* w, int32_t h_i, int32_t topk, int32_t* out_idx, const void* q_sfa_bf16,
+                    int32_t h_s, float sm_scale, void* out_bf16, float* out_lse, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  // every argument is checked before anything is launched
+  if (n_new < 0) return fail(DSA_ERR_INVALID_ARG, "decode_step: n_new < 0");
+  if (num_pages < 1 || num_pages > INT64_MAX / DSA_PAGE_SIZE)
+    return fail(DSA_ERR_INVALID_ARG, "decode_step: num_pages must be >= 1");
+  if (n_new > 0) {
+    if (!k_new_bf16 || !kv_new_bf16 || !slot_mapping || !k_cache || !kv_cache)
+      return fail(DSA_ERR_INVALID_ARG, "decode_step: null pointer among the new tokens or caches");
+    if (!aligned(k_new_bf16, 16) || !aligned(kv_new_bf16, 16) || !aligned(k_cache, 16) || !aligned(kv_cache, 16) ||
+        !aligned(slot_mapping, 8))
+      return fail(DSA_ERR_INVALID_ARG, "decode_step: rows and caches must be 16-byte aligned");
+  }
+  int rc = check_indexer("decode_step", q_idx_bf16, w, n_q, h_i, q_group, k_cache, num_pages, page_table,
+                         max_pages, seq_lens, q_seq, q_pos, n_seq, max_ctx);
+  if (rc) return rc;
+  if (topk < 1 || topk > 2048) return fail(DSA_ERR_UNSUPPORTED, "decode_step: topk must be 1..2048");
+  if (h_s < 1 || h_s > 128) return fail(DSA_ERR_UNSUPPORTED, "decode_step: h_s must be 1..128");
+  if (!(sm_scale > 0.f) || sm_scale != sm_scale) return fail(DSA_ERR_INVALID_ARG, "decode_step: sm_scale must be positive");
+  if (n_q > 0) {
+    if (!out_idx || !q_sfa_bf16 || !kv_cache || !out_bf16) return fail(DSA_ERR_INVALID_ARG, "decode_step: null pointer");
+    if (!aligned(q_sfa_bf16, 16) || !aligned(kv_cache, 16) || !aligned(out_bf16, 16))
+      return fail(DSA_ERR_INVALID_ARG, "decode_step: q_sfa, kv_cache and out must be 16-byte aligned");
+    const size_t need = dsa::sfa_workspace_bytes(n_q, h_s, topk);
+    if (need && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
+      return fail(DSA_ERR_INVALID_ARG, "decode_step: workspace must be >= %zu bytes and 256-byte aligned", need);
+  }
+  if (n_new == 0 && n_q == 0) return DSA_OK;  // nothing to launch
+  unsigned* st = status_ptr();
+  if (!st) return fail(DSA_ERR_CUDA, "decode_step: no CUDA device");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = dsa::launch_quant_both(k_new_bf16, kv_new_bf16, slot_mapping, n_new, k_cache, kv_cache,
+                                         num_pages * DSA_PAGE_SIZE, st, s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode_step: cache writer launch");
+  if (n_q == 0) return DSA_OK;
+  dsa::IndexerArgs ia{q_idx_bf16, w, n_q, h_i, q_group, k_cache, num_pages, page_table, max_pages,
+                      seq_lens, q_seq, q_pos, n_seq, max_ctx, topk, out_idx, nullptr, nullptr, st};
+  ia.early_inputs = n_new > 0 ? 1 : 0;  // the writer launched just above precedes the indexer
+  const char* why = nullptr;
+  e = dsa::launch_indexer(ia, s, &why);
+  if (e != cudaSuccess) return why ? fail(DSA_ERR_UNSUPPORTED, "%s", why) : cuda_fail(e, "decode_step: indexer launch");
+  dsa::SfaArgs sa{q_sfa_bf16, n_q, h_s, kv_cache, num_pages, page_table, max_pages, seq_lens, q_seq, n_seq,
+                  out_idx, topk, sm_scale, out_bf16, out_lse, workspace, workspace_bytes, st};
+  e = dsa::launch_sfa(sa, s, &why);
+  if (e != cudaSuccess) return why ? fail(DSA_ERR_UNSUPPORTED, "%s", why) : cuda_fail(e, "decode_step: sparse_attn launch");
   return DSA_OK;
 }
 

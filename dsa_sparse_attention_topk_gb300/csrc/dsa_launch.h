@@ -52,6 +52,10 @@ struct IndexerArgs {
   float* out_scores;         // [n_q][topk] or null
   float* out_full;           // [n_q][max_ctx] (scores mode) or null
   unsigned* status;
+  // 1: the previous kernel on the stream is this library's cache writer, which signals its
+  // dependents only after its own wait; everything but the K-cache is then complete when
+  // the indexer starts, and only the K-cache copies wait for the writer
+  int early_inputs = 0;
 };
 
 struct SfaArgs {

@@ -163,20 +163,23 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
   topk_init(tk);
   for (int i = tid; i < G * kHistBins; i += kThreads) s_hist0[i] = 0;
   pdl_launch_dependents();
-  pdl_wait();  // nothing global is touched before the previous kernel on the stream is done
+  // nothing global is read before the previous kernel on the stream is done, unless that
+  // kernel is the cache writer of a decode step (early_inputs): then only the K-cache, the
+  // writer's output, waits (the producer lanes, below); the reads before it bypass L1
+  if (!a.early_inputs) pdl_wait();
   if (tid == 0) {
-    int seq = a.q_seq[row0];
+    int seq = __ldcg(a.q_seq + row0);
     unsigned bad = 0;
     if (seq < 0 || seq >= a.n_seq) { bad |= DSA_STATUS_BAD_SEQ; seq = -1; }
     int L = 0;
     if (seq >= 0) {
-      L = a.seq_lens[seq];
+      L = __ldcg(a.seq_lens + seq);
       if (L < 0 || L > a.max_ctx) { bad |= DSA_STATUS_BAD_LEN; L = L < 0 ? 0 : a.max_ctx; }
     }
     int n_max = 0;
     for (int j = 0; j < G; ++j) {
-      if (a.q_seq[row0 + j] != a.q_seq[row0]) bad |= DSA_STATUS_BAD_SEQ;
-      long long n = static_cast<long long>(a.q_pos[row0 + j]) + 1;
+      if (__ldcg(a.q_seq + row0 + j) != seq && seq >= 0) bad |= DSA_STATUS_BAD_SEQ;
+      long long n = static_cast<long long>(__ldcg(a.q_pos + row0 + j)) + 1;
       n = n < 0 ? 0 : (n > L ? L : n);
       bs.n_sel[j] = static_cast<int>(n);
       n_max = n > n_max ? static_cast<int>(n) : n_max;
@@ -199,7 +202,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
   if (warp == 0 && lane >= 1 && lane <= 16) {
     // warm L2 with the sequence's page-table row (one 128-byte line per lane) while lane 0
     // reads the sequence information, so the producer's page lookups skip a DRAM access
-    const int sq = a.q_seq[row0];
+    const int sq = __ldcg(a.q_seq + row0);
     if (sq >= 0 && sq < a.n_seq) {
       const int32_t* prow = a.page_table + static_cast<size_t>(sq) * a.max_pages;
       const int i = 32 * (lane - 1);
@@ -226,7 +229,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
 
   auto phys_page = [&](int lp) -> int {
     if (seq < 0 || lp >= n_pages_needed || lp >= a.max_pages) return -1;
-    const int pg = ptab[lp];
+    const int pg = __ldcg(ptab + lp);
     return (pg >= 0 && pg < a.num_pages) ? pg : -2;
   };
   // physical page of each of this chunk's logical pages (-1 past the end, -2 invalid),
@@ -239,6 +242,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
     __syncwarp();
     tc::mbar_arrive(&bs.pages_ready);
     if (lane < kProd) {
+      if (a.early_inputs) pdl_wait();  // the K-cache copies follow the cache writer
       // lane l issues tiles t = l (mod kProd): one thread alone cannot issue copies fast
       // enough to keep the HBM busy, and with a ring of a multiple of kProd stages each
       // stage keeps one issuer
@@ -277,7 +281,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
 #pragma unroll
     for (int r = 0; r < kWPer; ++r) {
       const int i = tid - 32 + r * (kThreads - 32), j = i / Hp, h = i % Hp;
-      wv[r] = (i < G * Hp && h < H) ? a.w[static_cast<size_t>(row0 + j) * H + h] : 0.f;
+      wv[r] = (i < G * Hp && h < H) ? __ldcg(a.w + static_cast<size_t>(row0 + j) * H + h) : 0.f;
     }
     for (int n0 = warp - 1; n0 < Np; n0 += kPrepWarps * kBatch) {
       uint2 raw[kBatch];
@@ -286,8 +290,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
         const int n = n0 + k * kPrepWarps;
         raw[k] = make_uint2(0u, 0u);
         if (n < Np && (n % Hp) < H)
-          raw[k] = *reinterpret_cast<const uint2*>(qbase + (static_cast<size_t>(row0 + n / Hp) * H + (n % Hp)) * kIdxDim +
-                                                   4 * lane);
+          raw[k] = __ldcg(reinterpret_cast<const uint2*>(qbase + (static_cast<size_t>(row0 + n / Hp) * H + (n % Hp)) * kIdxDim +
+                                                         4 * lane));
       }
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
@@ -406,6 +410,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
                        a.out_idx + row * a.topk, a.out_scores ? a.out_scores + row * a.topk : nullptr, cand, cand_cap);
     }
   }
+  // every CTA has waited for the writer before it leaves, so this grid never completes
+  // before the writer does (the next kernel relies on that for the latent cache)
+  if (a.early_inputs && tid == 0) pdl_wait();
   cluster_sync();  // no CTA leaves while its shared memory may still be addressed
   tc::fence_after_sync();
   if (warp == 1) tc::tmem_dealloc(tmem, pl.tmem_cols);

@@ -170,8 +170,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 quant_both_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ kv,
                   const int64_t* __restrict__ slots, int n_tokens, uint8_t* __restrict__ k_cache,
                   uint8_t* __restrict__ kv_cache, int64_t num_slots, unsigned* status) {
-  pdl_launch_dependents();
+  // dependents are signalled only after the wait: once a dependent starts, every kernel
+  // before this one is complete (a decode step's indexer reads its other inputs early)
   pdl_wait();
+  pdl_launch_dependents();
   DSA_FOR_TOKENS(t) {
     const KTok kin = load_k_token(k, slots, t);
     const KvTok kvin = load_kv_token(kv, slots, t);

@@ -5,7 +5,7 @@ computation is a call into the C ABI.
 
 import torch
 
-from . import (alloc_k_cache, alloc_kv_cache, quant_kv_mxfp8, quant_kv_fp8, quant_kv, indexer_topk,
+from . import (alloc_k_cache, alloc_kv_cache, quant_kv_mxfp8, quant_kv_fp8, decode_step, indexer_topk,
                sparse_attn, sparse_attn_workspace_size)
 
 
@@ -58,18 +58,16 @@ class DsaDecodeLayer:
 
     def step(self, k_new, kv_new, slots_new, q_idx, w, q_sfa, page_table, seq_lens, q_seq, q_pos,
              max_ctx, q_group=1):
-        """Write this step's tokens (both caches, one launch), then decode.
-
-        The three launches go on the current stream, one after the other: the library
-        launches with programmatic dependent launch, so each kernel's launch and set-up
-        overlap the end of the one before.
+        """Write this step's tokens into both caches, then decode: one library call
+        (dsa_decode_step), which launches the cache writer, the indexer and SFA on the
+        current stream with programmatic dependent launch, so each kernel's set-up overlaps
+        the end of the one before, and the indexer reads its other inputs while the writer
+        runs.
         """
-        main = torch.cuda.current_stream(self.device)
-        quant_kv(k_new, kv_new, slots_new, self.k_cache, self.kv_cache, stream=main)
         n_q = q_idx.shape[0]
         b = self._buffers(n_q)
-        indexer_topk(q_idx, w, self.k_cache, page_table, seq_lens, q_seq, q_pos, self.topk, max_ctx,
-                     q_group=q_group, out_idx=b["idx"], stream=main)
-        sparse_attn(q_sfa, self.kv_cache, page_table, seq_lens, q_seq, b["idx"], self.sm_scale,
-                    out=b["out"], out_lse=b["lse"], workspace=b["ws"], stream=main)
+        decode_step(k_new, kv_new, slots_new, self.k_cache, self.kv_cache, q_idx, w, q_sfa, page_table,
+                    seq_lens, q_seq, q_pos, self.topk, max_ctx, self.sm_scale, q_group=q_group,
+                    out_idx=b["idx"], out=b["out"], out_lse=b["lse"], workspace=b["ws"],
+                    stream=torch.cuda.current_stream(self.device))
         return b["out"], b["lse"], b["idx"]

@@ -200,6 +200,32 @@ int dsa_sparse_attn(const void* q_bf16, int32_t n_q, int32_t h_s, const uint8_t*
                     float* out_lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * dsa_decode_step -- one decode step of a DSA layer in one call: dsa_quant_kv for the
+ * step's new tokens, then dsa_indexer_topk, then dsa_sparse_attn over its out_idx, on
+ * `stream`, with the results each of those calls gives.  The pages describe the two
+ * stages and the cache writes, not this packaging.  Because the library launches the
+ * three kernels itself, it knows that the cache writer precedes the indexer: the indexer
+ * then reads its queries, weights, sequence information and page table while the writer
+ * is still running, and only its K-cache copies wait for the writer (a separate
+ * dsa_indexer_topk call cannot assume that).
+ *   k_new_bf16, kv_new_bf16, slot_mapping, n_new   as for dsa_quant_kv (n_new may be 0:
+ *                        nothing is written, and the indexer waits as usual).
+ *   k_cache, kv_cache    both caches, num_pages pages each (slots 0 .. 64 num_pages - 1).
+ *   page_table .. q_group, q_idx_bf16, w, h_i, topk, out_idx   as for dsa_indexer_topk
+ *                        (out_scores is not produced).
+ *   q_sfa_bf16, h_s, sm_scale, out_bf16, out_lse, workspace, workspace_bytes   as for
+ *                        dsa_sparse_attn (topk_idx is out_idx).
+ * Every argument is checked before anything is launched; errors as for the three calls.
+ */
+int dsa_decode_step(const void* k_new_bf16, const void* kv_new_bf16, const int64_t* slot_mapping, int32_t n_new,
+                    uint8_t* k_cache, uint8_t* kv_cache, int64_t num_pages, const int32_t* page_table,
+                    int32_t max_pages, const int32_t* seq_lens, int32_t n_seq, int32_t max_ctx, int32_t n_q,
+                    const int32_t* q_seq, const int32_t* q_pos, int32_t q_group, const void* q_idx_bf16,
+                    const float* w, int32_t h_i, int32_t topk, int32_t* out_idx, const void* q_sfa_bf16,
+                    int32_t h_s, float sm_scale, void* out_bf16, float* out_lse, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/*
  * dsa_sparse_attn_noalloc -- dsa_sparse_attn for callers that cannot allocate device
  * memory.  The pages have no counterpart: this is a convenience of this library.
  * Some callers have no allocator they may use for the split-merge workspace -- code that

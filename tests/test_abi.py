@@ -105,3 +105,34 @@ def test_workspace_size_is_host_only(dsa):
     n = dsa.lib().dsa_sparse_attn_workspace_size(32, 128, 2048)
     assert n >= 0
     assert dsa.lib().dsa_sparse_attn_workspace_size(0, 128, 2048) == 0
+
+
+def _step_call(lib, **kw):
+    P = ctypes.c_void_p
+    a = dict(k_new=1, kv_new=1, slots=1, n_new=2, k_cache=1, kv_cache=1, num_pages=4, pt=1, max_pages=4,
+             seq_lens=1, n_seq=1, max_ctx=256, n_q=1, q_seq=1, q_pos=1, q_group=1, q_idx=1, w=1, h_i=64,
+             topk=16, out_idx=1, q_sfa=1, h_s=128, sm_scale=0.07, out=1, lse=None, ws=1, ws_bytes=1 << 30)
+    a.update(kw)
+    p = lambda v: None if v is None else P(v * 256)
+    return lib.dsa_decode_step(p(a["k_new"]), p(a["kv_new"]), p(a["slots"]), a["n_new"], p(a["k_cache"]),
+                               p(a["kv_cache"]), a["num_pages"], p(a["pt"]), a["max_pages"], p(a["seq_lens"]),
+                               a["n_seq"], a["max_ctx"], a["n_q"], p(a["q_seq"]), p(a["q_pos"]), a["q_group"],
+                               p(a["q_idx"]), p(a["w"]), a["h_i"], a["topk"], p(a["out_idx"]), p(a["q_sfa"]),
+                               a["h_s"], ctypes.c_float(a["sm_scale"]), p(a["out"]), p(a["lse"]), p(a["ws"]),
+                               a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_new=-1), -1), (dict(kv_new=None), -1), (dict(num_pages=0), -1), (dict(h_i=65), -2),
+    (dict(topk=4096), -2), (dict(h_s=129), -2), (dict(sm_scale=0.0), -1), (dict(out=None), -1),
+    (dict(q_sfa=None), -1), (dict(ws=None, topk=2048), -1), (dict(n_q=3, q_group=2), -1),
+])
+def test_decode_step_rejects_bad_arguments_before_launching(dsa, kw, code):
+    lib = dsa.lib()
+    assert _step_call(lib, **kw) == code
+    assert lib.dsa_last_error()
+
+
+def test_decode_step_with_nothing_to_do(dsa):
+    # no new tokens and no query rows: nothing to launch
+    assert _step_call(dsa.lib(), n_new=0, n_q=0, k_new=None, kv_new=None, slots=None) == 0

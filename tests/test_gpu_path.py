@@ -126,3 +126,53 @@ def test_repeated_calls_with_l2_flush_stay_clean(dsa):
         assert torch.equal(idx, idx0) and torch.equal(val, val0)
         assert torch.equal(full, full0) and torch.equal(out, out0)
     assert dsa.device_status() == 0
+
+
+def _step_inputs(wl, dw):
+    """The rows of the query tokens themselves (the step's new tokens) and their slots."""
+    k_new, kv_new, s_new = [], [], []
+    for b in range(wl.B):
+        pos = wl.q_pos[wl.q_seq == b]
+        if pos.size == 0:
+            continue
+        k_new.append(wl.k_seq(b, dw.q_idx_cpu, dw.w_cpu)[pos])
+        kv_new.append(wl.kv_seq(b)[pos])
+        s_new.append(torch.from_numpy(wl.slot_mapping(b)[pos]))
+    return (torch.cat(k_new).cuda(), torch.cat(kv_new).cuda(), torch.cat(s_new).cuda())
+
+
+@pytest.mark.parametrize("name", ["tiny", "mtp", "decode_b32_ctx32k"])
+def test_decode_step_equals_the_three_calls(dsa, name):
+    # dsa_decode_step writes the new tokens and decodes in one call; its indexer reads all
+    # but the K-cache before the writer finishes.  The new tokens' cache slots are wiped
+    # first, so a K-cache read that overtook the writer would change the selection.
+    wl = (W.custom([1000, 3000, 2], per_seq=2, h_i=64, h_s=64, topk=512, seed=8) if name == "mtp"
+          else W.make(name))
+    dw = DeviceWorkload(wl)
+    k_new, kv_new, s_new = _step_inputs(wl, dw)
+    kc0, vc0 = dw.k_cache.clone(), dw.kv_cache.clone()
+    for kc, vc in ((kc0, vc0),):
+        pages = kc.view(-1, 8448)
+        for s in s_new.tolist():
+            pages[s // 64, (s % 64) * 128:(s % 64) * 128 + 128] = 0x7E    # codes -> +448
+            pages[s // 64, 8192 + (s % 64) * 4:8192 + (s % 64) * 4 + 4] = 0xFE   # scales -> 2^127
+            vc.view(-1, 608)[s] = 0x7E
+    # the three calls on one copy of the wiped caches
+    ka, va = kc0.clone(), vc0.clone()
+    dsa.quant_kv(k_new, kv_new, s_new, ka, va)
+    idx_a, _ = dsa.indexer_topk(dw.q_idx, dw.w, ka, dw.page_table, dw.seq_lens, dw.q_seq, dw.q_pos, wl.topk,
+                                wl.max_ctx, q_group=wl.q_group)
+    lse_a = torch.empty(wl.n_q, wl.h_s, dtype=torch.float32, device="cuda")
+    out_a, _ = dsa.sparse_attn(dw.q_sfa, va, dw.page_table, dw.seq_lens, dw.q_seq, idx_a, wl.sm_scale,
+                               out_lse=lse_a)
+    # one decode step on another
+    kb, vb = kc0.clone(), vc0.clone()
+    lse_b = torch.empty(wl.n_q, wl.h_s, dtype=torch.float32, device="cuda")
+    out_b, _, idx_b = dsa.decode_step(k_new, kv_new, s_new, kb, vb, dw.q_idx, dw.w, dw.q_sfa, dw.page_table,
+                                      dw.seq_lens, dw.q_seq, dw.q_pos, wl.topk, wl.max_ctx, wl.sm_scale,
+                                      q_group=wl.q_group, out_lse=lse_b)
+    assert dsa.device_status() == 0
+    assert torch.equal(ka, kb) and torch.equal(va, vb)
+    assert torch.equal(ka, dw.k_cache) and torch.equal(va, dw.kv_cache)   # the wipe was undone
+    assert torch.equal(idx_a, idx_b)
+    assert torch.equal(out_a, out_b) and torch.equal(lse_a, lse_b)
