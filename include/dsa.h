@@ -2,15 +2,15 @@
  * dsa.h -- C ABI of the GB300 (sm_103a) DeepSeek-style Sparse Attention decode path.
  *
  * The path has two stages, as described on "Deep Dive into Sparse Attention and
- * Engineering Optimizations for Efficient Inference in Kimi K3.1 Pro" (section 1, the
- * two-stage "coarse filtering first, precise computation second" scheme):
+ * Engineering Optimizations for Efficient Inference in Kimi K3.1 Pro" (section 1: a cheap
+ * pass picks the positions, then exact attention runs only on those):
  *   1. a fused Lightning Indexer that reads an MXFP8 K-cache straight from its pages,
  *      scores every selectable past position and keeps the Top-K on chip
  *      (dsa_indexer_topk);
  *   2. Sparse Flash Attention that gathers the selected entries of a paged FP8 MLA
  *      latent cache and runs online-softmax attention over them (dsa_sparse_attn).
  * Two cache writers fill the caches (dsa_quant_kv_mxfp8, dsa_quant_kv_fp8; dsa_quant_kv
- * runs both in one launch).
+ * runs both in one launch), and dsa_decode_step runs a whole decode step in one call.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
