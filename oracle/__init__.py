@@ -38,7 +38,7 @@ from .quant import (
     FP8_TILE,
 )
 from .indexer import indexer_scores_row, topk_row, indexer_topk_rows
-from .sfa import sparse_attention_row, sparse_attention_rows
+from .sfa import sparse_attention_row
 from .pipeline import decode_rows
 
 __all__ = [
@@ -46,6 +46,6 @@ __all__ = [
     "mxfp8_quantize", "mxfp8_dequantize", "fp8_tile_quantize", "fp8_tile_dequantize",
     "MX_GROUP", "FP8_TILE",
     "indexer_scores_row", "topk_row", "indexer_topk_rows",
-    "sparse_attention_row", "sparse_attention_rows",
+    "sparse_attention_row",
     "decode_rows",
 ]

@@ -9,7 +9,8 @@ Passages followed:
   Hardware", section "Lightning Indexer Three-Stream Coordination": the indexer performs
   relevance scoring, head-weight weighting and Top-K index selection.
 
-The pages print no formula.  The reading adopted (stated in the design doc) is
+The pages print no formula.  The reading adopted here is the plainest one that names both
+steps, a per-head relevance score and a weighting of the heads, with no extra scale:
 
     score[t, p] = sum_h  w[t, h] * max(0, q_hat[t, h, :] . k_hat[p, :])
 

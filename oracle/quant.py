@@ -10,7 +10,7 @@
   Per-Token-Head-Tile Quantization for SFA" -- one scaling factor per 128-element tile
   of each token (and head; the MLA latent cache has a single KV head).
 
-Readings adopted where the pages are silent (each listed in the design doc):
+Readings adopted where the pages are silent:
 
 * MX scale rule: the OCP MX v1.0 rule, shared exponent e = floor(log2(amax)) - 8
   (8 = the largest exponent of E4M3), clamped to [-127, 127], stored as E8M0 code e+127;

@@ -13,7 +13,8 @@ Passages followed:
   Hardware", section "Preserving a Mixed-Precision Path": the query and the final
   attention weighting stay BF16; only the cache is FP8.
 
-Reading adopted (absorbed MLA decode; the design doc lists it): each selected position j
+Reading adopted (absorbed MLA decode, the form the workloads' 576-wide latent with a
+512-wide value implies): each selected position j
 carries one dequantised latent row kv_hat[j] of width 576 that serves as the key, and
 its first 512 entries serve as the value.  For query row t and head h over the valid
 (non -1) selected entries J:
@@ -48,14 +49,4 @@ def sparse_attention_row(q, kv_hat, idx, sm_scale):
     l = p.sum(axis=1, keepdims=True)
     o = (p @ kv[:, :D_V]) / l
     lse = (m + np.log(l))[:, 0]
-    return o, lse
-
-
-def sparse_attention_rows(q, kv_hat_of_row, idx, sm_scale):
-    """Several rows: q (R, H, 576); kv_hat_of_row: list of (n_r, 576); idx (R, K)."""
-    R, H, _ = q.shape
-    o = np.zeros((R, H, D_V))
-    lse = np.zeros((R, H))
-    for r in range(R):
-        o[r], lse[r] = sparse_attention_row(q[r], kv_hat_of_row[r], idx[r], sm_scale)
     return o, lse

@@ -8,7 +8,8 @@ import pytest
 import torch
 
 from oracle.quant import mxfp8_quantize, mxfp8_dequantize
-from oracle.indexer import indexer_scores_row, topk_row, selectable_count, indexer_topk_rows
+from oracle.indexer import (indexer_scores_row, indexer_magnitude_row, topk_row, selectable_count,
+                            indexer_topk_rows)
 from oracle.pipeline import decode_rows
 
 # Hand example (tests/golden/indexer_hand_2h8p.json): only the first four of the 128
@@ -42,6 +43,24 @@ def test_hand_dots():
 def test_hand_scores(case):
     s = indexer_scores_row(_deq(Q), np.array(case["w"]), _deq(K8))
     assert s.tolist() == case["scores"]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_hand_magnitude(case):
+    # the denominator of every score tolerance and of the Top-K tie band: hand values that
+    # a dropped abs on w, an abs taken after the head sum, or a ReLU applied to it would miss
+    m = indexer_magnitude_row(_deq(Q), np.array(case["w"]), _deq(K8))
+    assert m.tolist() == case["magnitude"]
+
+
+def test_magnitude_bounds_score():
+    # |score| <= magnitude always, with equality when every weight and dot is >= 0
+    rng = np.random.default_rng(5)
+    q, k, w = rng.standard_normal((4, 128)), rng.standard_normal((50, 128)), rng.standard_normal(4)
+    s, m = indexer_scores_row(q, w, k), indexer_magnitude_row(q, w, k)
+    assert np.all(np.abs(s) <= m * (1 + 1e-12))
+    qp, kp, wp = np.abs(q), np.abs(k), np.abs(w)
+    assert np.allclose(indexer_scores_row(qp, wp, kp), indexer_magnitude_row(qp, wp, kp), rtol=1e-12)
 
 
 @pytest.mark.parametrize("case", CASES)
