@@ -34,7 +34,7 @@ V_DIM = 512
 KCACHE_PAGE_BYTES = 8448
 KVCACHE_TOKEN_BYTES = 608
 
-STATUS_BITS = {1: "BAD_PAGE", 2: "BAD_SEQ", 4: "BAD_LEN", 8: "BAD_INDEX", 16: "TIMEOUT"}
+STATUS_BITS = {1: "BAD_PAGE", 2: "BAD_SEQ", 4: "BAD_LEN", 8: "BAD_INDEX", 16: "TIMEOUT", 32: "NAN_SCORE"}
 
 _lib = None
 
@@ -70,6 +70,7 @@ _SIGS = {
                                        _P, _P, _I32, _P, _P, _I32, _I32, _P, _P, _I32, _F32, _P, _P, _P, _SZ,
                                        _P]),
     "dsa_device_status": (ctypes.c_int, [_P]),
+    "dsa_test_stall_indexer": (ctypes.c_int, [_I32]),
     "dsa_last_error": (ctypes.c_char_p, []),
     "dsa_version": (ctypes.c_int, []),
 }
@@ -267,6 +268,13 @@ def device_status(stream=None):
     if rc < 0:
         _check(rc)
     return rc
+
+
+def test_stall_indexer(wait_limit_us):
+    """Testing aid for the bounded waits (dsa_test_stall_indexer): a positive limit makes
+    every following indexer launch stall its copy producer and give up waiting after that
+    many microseconds; 0 restores normal operation."""
+    _check(lib().dsa_test_stall_indexer(int(wait_limit_us)))
 
 
 def status_names(bits):

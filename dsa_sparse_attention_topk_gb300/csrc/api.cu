@@ -2,6 +2,7 @@
 // the per-thread error message.  Every compute step runs in the kernels behind
 // dsa_launch.h; nothing here touches tensor data on the host.
 
+#include <atomic>
 #include <cstdint>
 #include <cstdarg>
 #include <cstdio>
@@ -49,7 +50,47 @@ unsigned* status_ptr() {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// dsa_test_stall_indexer: 0 = normal operation, else the waits' limit in microseconds with
+// the indexer's copy producer stalled
+std::atomic<int> g_stall_wait_us{0};
+
+void apply_test_hooks(dsa::IndexerArgs& a) {
+  const int us = g_stall_wait_us.load(std::memory_order_relaxed);
+  if (us > 0) {
+    a.wait_ns = static_cast<uint64_t>(us) * 1000ull;
+    a.stall_producer = 1;
+  }
+}
+
 }  // namespace
+
+bool dsa::device_info(DevInfo* out, const char** err) {
+  static std::mutex mu;
+  static DevInfo cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    *err = "no current CUDA device";
+    return false;
+  }
+  if (dev < 0 || dev >= 64) {
+    *err = "device ordinal out of range (the library serves ordinals 0..63)";
+    return false;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  DevInfo& d = cache[dev];
+  if (!d.n_sm) {
+    DevInfo q;
+    if (cudaDeviceGetAttribute(&q.n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&q.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        q.n_sm <= 0) {
+      *err = "device attribute query failed";
+      return false;
+    }
+    d = q;
+  }
+  *out = d;
+  return true;
+}
 
 extern "C" {
 
@@ -144,6 +185,7 @@ int dsa_indexer_topk(const void* q_bf16, const float* w, int32_t n_q, int32_t h_
   if (!st) return fail(DSA_ERR_CUDA, "indexer_topk: no CUDA device");
   dsa::IndexerArgs a{q_bf16, w, n_q, h_i, q_group, k_cache, num_pages, page_table, max_pages,
                      seq_lens, q_seq, q_pos, n_seq, max_ctx, topk, out_idx, out_scores, nullptr, st};
+  apply_test_hooks(a);
   const char* why = nullptr;
   cudaError_t e = dsa::launch_indexer(a, static_cast<cudaStream_t>(stream), &why);
   if (e != cudaSuccess) return why ? fail(DSA_ERR_UNSUPPORTED, "%s", why) : cuda_fail(e, "indexer_topk launch");
@@ -164,6 +206,7 @@ int dsa_indexer_scores(const void* q_bf16, const float* w, int32_t n_q, int32_t 
   if (!st) return fail(DSA_ERR_CUDA, "indexer_scores: no CUDA device");
   dsa::IndexerArgs a{q_bf16, w, n_q, h_i, q_group, k_cache, num_pages, page_table, max_pages,
                      seq_lens, q_seq, q_pos, n_seq, max_ctx, 1, nullptr, nullptr, out_scores, st};
+  apply_test_hooks(a);
   const char* why = nullptr;
   cudaError_t e = dsa::launch_indexer(a, static_cast<cudaStream_t>(stream), &why);
   if (e != cudaSuccess) return why ? fail(DSA_ERR_UNSUPPORTED, "%s", why) : cuda_fail(e, "indexer_scores launch");
@@ -246,6 +289,7 @@ int dsa_decode_step(const void* k_new_bf16, const void* kv_new_bf16, const int64
   dsa::IndexerArgs ia{q_idx_bf16, w, n_q, h_i, q_group, k_cache, num_pages, page_table, max_pages,
                       seq_lens, q_seq, q_pos, n_seq, max_ctx, topk, out_idx, nullptr, nullptr, st};
   ia.early_inputs = n_new > 0 ? 1 : 0;  // the writer launched just above precedes the indexer
+  apply_test_hooks(ia);
   const char* why = nullptr;
   e = dsa::launch_indexer(ia, s, &why);
   if (e != cudaSuccess) return why ? fail(DSA_ERR_UNSUPPORTED, "%s", why) : cuda_fail(e, "decode_step: indexer launch");
@@ -287,6 +331,13 @@ int dsa_sparse_attn_noalloc(const void* q_bf16, int32_t n_q, int32_t h_s, const 
   cudaError_t e = dsa::launch_sfa_noalloc(a, static_cast<cudaStream_t>(stream), &why);
   if (e != cudaSuccess)
     return why ? fail(DSA_ERR_UNSUPPORTED, "%s", why) : cuda_fail(e, "sparse_attn_noalloc launch");
+  return DSA_OK;
+}
+
+int dsa_test_stall_indexer(int32_t wait_limit_us) {
+  if (wait_limit_us < 0 || wait_limit_us > 10000000)
+    return fail(DSA_ERR_INVALID_ARG, "test_stall_indexer: wait_limit_us must be 0..10000000");
+  g_stall_wait_us.store(wait_limit_us, std::memory_order_relaxed);
   return DSA_OK;
 }
 

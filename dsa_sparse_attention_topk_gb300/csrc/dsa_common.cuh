@@ -70,10 +70,21 @@ __device__ __forceinline__ int mx_shared_exp(float amax) {
 // ---------------------------------------------------------------------------------
 // Score keys: an order-preserving map float -> uint32 (larger score, larger key).
 // -0 is folded onto +0 so equal scores get equal keys.  Key 0 marks "not selectable".
+// Every NaN, whatever its sign or payload, maps to key 1: below every other score (a
+// stable descending sort puts NaN last), so NaN scores are kept only when fewer than K
+// others are selectable, lowest positions first.
+constexpr uint32_t kNanKey = 1u;
 __device__ __forceinline__ uint32_t score_key(float s) {
+  if (s != s) return kNanKey;
   s = s + 0.0f;  // -0 -> +0
   uint32_t b = __float_as_uint(s);
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+// max(x, 0) that keeps NaN (fmaxf would return 0 for a NaN x).
+__device__ __forceinline__ float relu_nan(float x) {
+  float y;
+  asm("max.NaN.f32 %0, %1, 0f00000000;" : "=f"(y) : "f"(x));
+  return y;
 }
 __device__ __forceinline__ float key_score(uint32_t k) {
   uint32_t b = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;

@@ -36,6 +36,14 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
+// Multiprocessor count and opt-in shared memory per block of the current device, queried
+// once per device (under a lock) and cached for the life of the process.  Returns false
+// (with `err` set) when there is no current device or its ordinal is 64 or more.
+struct DevInfo {
+  int n_sm = 0, smem_optin = 0;
+};
+bool device_info(DevInfo* out, const char** err);
+
 struct IndexerArgs {
   const void* q;             // bf16 [n_q][h_i][128]
   const float* w;            // [n_q][h_i]
@@ -56,6 +64,10 @@ struct IndexerArgs {
   // dependents only after its own wait; everything but the K-cache is then complete when
   // the indexer starts, and only the K-cache copies wait for the writer
   int early_inputs = 0;
+  // testing aid for the bounded waits (dsa_test_stall_indexer): the waits' limit, and 1 to
+  // make the copy-issuing lanes stop before their first copy
+  uint64_t wait_ns = 1000000000ull;
+  int stall_producer = 0;
 };
 
 struct SfaArgs {

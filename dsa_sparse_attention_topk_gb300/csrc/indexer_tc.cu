@@ -75,6 +75,7 @@ struct Barriers {
   uint64_t pages_ready;
   uint64_t tfull[kMaxAcc];
   uint64_t tempty[kMaxAcc];
+  uint64_t drain[kMaxAcc];  // after an abort: the issuer's own MMAs have completed
   uint32_t tmem_base;
   int abort;
   int seq;
@@ -196,6 +197,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
     for (int i = 0; i < kNacc; ++i) {
       tc::mbar_init(&bs.tfull[i], 1);
       tc::mbar_init(&bs.tempty[i], 128);
+      tc::mbar_init(&bs.drain[i], 1);
     }
     tc::mbar_fence_init();
   }
@@ -226,6 +228,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
   const int32_t* ptab = a.page_table + static_cast<size_t>(seq < 0 ? 0 : seq) * a.max_pages;
   const uint32_t tmem = bs.tmem_base;
   volatile int* abort = &bs.abort;
+  const uint64_t wait_ns = a.wait_ns;
 
   auto phys_page = [&](int lp) -> int {
     if (seq < 0 || lp >= n_pages_needed || lp >= a.max_pages) return -1;
@@ -247,9 +250,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
       // enough to keep the HBM busy, and with a ring of a multiple of kProd stages each
       // stage keeps one issuer
       if (lane == 0) tc::prefetch_tmap(&kmap);
-      for (int t = lane; t < ntiles; t += kProd) {
+      int last = -1;  // the last tile this lane issued
+      for (int t = a.stall_producer ? ntiles : lane; t < ntiles; t += kProd) {
         const int s = t % S, it = t / S;
-        tc::mbar_wait(&bs.empty[s], (it & 1) ^ 1, abort, a.status);
+        if (!tc::mbar_wait(&bs.empty[s], (it & 1) ^ 1, abort, a.status, wait_ns)) break;
         uint8_t* st = smem + pl.off_stage + s * kStageBytes;
         const int pg0 = s_pages[2 * t], pg1 = s_pages[2 * t + 1];
         if (pg0 == -2 || pg1 == -2) flag(a.status, DSA_STATUS_BAD_PAGE);
@@ -265,6 +269,13 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
           tc::bulk_load(st + kStageA + 256, a.k_cache + static_cast<int64_t>(pg1) * kKPageBytes + kKScaleOff, 256,
                         &bs.full[s]);
         }
+        last = t;
+      }
+      if (*abort) {
+        // copies may still be landing in the ring: wait for the newest phase of each stage
+        // this lane filled.  Its last S / kProd tiles sit in distinct stages (a lane's tiles
+        // are kProd apart and S is a multiple of kProd) that no other lane uses.
+        for (int t = last; t >= 0 && t > last - S; t -= kProd) tc::mbar_drain(&bs.full[t % S], (t / S) & 1, wait_ns);
       }
     }
   } else {
@@ -333,7 +344,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
       const int s = t % S, it = t / S;
       const int acc = t % kNacc, ia = t / kNacc;
       uint8_t* st = smem + pl.off_stage + s * kStageBytes;
-      tc::mbar_wait(&bs.full[s], it & 1, abort, a.status);
+      // (every lane waits; the warp leaves the loop together once a wait gives up)
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&bs.full[s], it & 1, abort, a.status, wait_ns))) break;
       // scales: position order -> [32 rows][4 words], word (i, j) = position 32 j + i
       const uint32_t* sf_nat = reinterpret_cast<const uint32_t*>(st + kStageA);
       uint32_t* sf_t = reinterpret_cast<uint32_t*>(st + kStageA + kStageSF);
@@ -341,7 +353,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
       *reinterpret_cast<uint4*>(sf_t + 4 * lane) = v;
       tc::fence_async_smem();
       __syncwarp();
-      tc::mbar_wait(&bs.tempty[acc], (ia & 1) ^ 1, abort, a.status);
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&bs.tempty[acc], (ia & 1) ^ 1, abort, a.status, wait_ns))) break;
       tc::fence_after_sync();
       if (lane == 0) {
         const uint32_t d = tmem + pl.d_col[acc];
@@ -356,15 +368,21 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
       }
       __syncwarp();
     }
+    if (*abort && lane == 0) {
+      // the epilogue no longer waits for this issuer's products: wait for them here
+      tc::commit(&bs.drain[mi]);
+      tc::mbar_drain(&bs.drain[mi], 0, wait_ns);
+    }
+    __syncwarp();
   } else if (warp > kMma) {
     // ---------------- epilogue: set i (four warps) drains accumulator i ----------------
     const int set = (warp - 1 - kMma) >> 2;    // which accumulator this warp drains
     const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
     const int m = quarter * 32 + lane;         // tile row = position offset in the tile
-    tc::mbar_wait(&bs.pages_ready, 0, abort, a.status);
+    tc::mbar_wait(&bs.pages_ready, 0, abort, a.status, wait_ns);
     for (int t = set; t < ntiles; t += kNacc) {
       const int acc = t % kNacc, ia = t / kNacc;
-      const bool ok = tc::mbar_wait(&bs.tfull[acc], ia & 1, abort, a.status);
+      const bool ok = tc::mbar_wait(&bs.tfull[acc], ia & 1, abort, a.status, wait_ns);
       tc::fence_after_sync();
       const int local = t * kTileP + m;
       const int p = c0 + local;
@@ -380,19 +398,22 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
         const float* wj = s_w + j * HP;
         float s4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains over the heads
 #pragma unroll
-        for (int h = 0; h < HP; ++h) s4[h & 3] = fmaf(wj[h], fmaxf(__uint_as_float(r[h]), 0.f), s4[h & 3]);
+        for (int h = 0; h < HP; ++h) s4[h & 3] = fmaf(wj[h], relu_nan(__uint_as_float(r[h])), s4[h & 3]);
         sc[j] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
       }
       tc::fence_before_sync();
       tc::mbar_arrive(&bs.tempty[acc]);
+      bool nan_seen = false;
 #pragma unroll
       for (int j = 0; j < G; ++j) {
         const bool valid = ok && page_ok && local < len && p < bs.n_sel[j];
         const uint32_t key = valid ? score_key(sc[j]) : 0u;
+        nan_seen |= key == kNanKey;
         s_keys[j * pl.chunk_cap + local] = key;
         hist_add_top_digit(s_hist0 + j * kHistBins, key);
         if (a.out_full && valid) a.out_full[static_cast<size_t>(row0 + j) * a.max_ctx + p] = sc[j];
       }
+      if (__any_sync(0xffffffffu, nan_seen) && lane == 0) flag(a.status, DSA_STATUS_NAN_SCORE);
     }
   }
   tc::fence_before_sync();
@@ -442,24 +463,10 @@ EncodeFn encode_fn() {
   return fn;
 }
 
-struct DevInfo {
-  int n_sm = 0, smem_optin = 0;
-};
-DevInfo dev_info() {
-  static DevInfo cache[64];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  DevInfo& d = cache[dev & 63];
-  if (!d.n_sm) {
-    cudaDeviceGetAttribute(&d.n_sm, cudaDevAttrMultiProcessorCount, dev);
-    cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  }
-  return d;
-}
-
 template <int G, int HP>
 cudaError_t launch_gh(const IndexerArgs& a, cudaStream_t s, const char** err) {
-  const DevInfo di = dev_info();
+  DevInfo di;
+  if (!device_info(&di, err)) return cudaErrorInvalidDevice;
   const int n_groups = a.n_q / G;
   const size_t limit = static_cast<size_t>(di.smem_optin) - 1024;  // room for the 1024-byte alignment
   auto cap_for = [&](int c) {

@@ -182,9 +182,13 @@ quant_both_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
   }
 }
 
+// one warp per token, at most 16 blocks per multiprocessor (the loop strides over the rest)
 int grid_for(int n_tokens) {
+  DevInfo di;
+  const char* why = nullptr;
+  const int cap = device_info(&di, &why) ? di.n_sm * 16 : 2048;
   int blocks = (n_tokens + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  return blocks < 152 * 16 ? (blocks < 1 ? 1 : blocks) : 152 * 16;
+  return blocks < cap ? (blocks < 1 ? 1 : blocks) : cap;
 }
 
 }  // namespace

@@ -36,12 +36,13 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Wait for the phase with the given parity to complete.  Gives up after ~1 s: sets
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // ~1 s
+// Wait for the phase with the given parity to complete.  Gives up after limit_ns: sets
 // *abort (shared) and the TIMEOUT status bit and returns false.  Once *abort is set every
 // later wait returns false at once, so all roles run to the end of their loops (and to
 // the cluster barriers) instead of hanging.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          unsigned* status) {
+                                          unsigned* status, uint64_t limit_ns = kWaitLimitNs) {
   if (*abort) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
@@ -49,12 +50,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 255u) {
       if (*abort) return false;
-      if (global_ns() - t0 > 1000000000ull) {
+      if (global_ns() - t0 > limit_ns) {
         *abort = 1;
         flag(status, DSA_STATUS_TIMEOUT);
         return false;
       }
     }
+  }
+}
+// After an abort: wait, at most limit_ns, for a phase that this thread's own copies or
+// MMAs complete (they are still in flight, and the CTA must not free what they write
+// into).  Returns false if the limit ran out.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 255u && global_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -139,8 +139,8 @@ __device__ __forceinline__ void block_pick(TopkSmem& sm, const uint32_t* hist, u
                                            uint32_t& above) {
   if (threadIdx.x < 32) {
     uint32_t dd, ab;
-    warp_pick(hist, need, dd, ab);
-    if (threadIdx.x == 0) { sm.pick[0] = dd; sm.pick[1] = ab; sm.pick[3] = hist[dd]; }
+    const bool found = warp_pick(hist, need, dd, ab);
+    if (threadIdx.x == 0) { sm.pick[0] = dd; sm.pick[1] = ab; sm.pick[2] = found ? 1u : 0u; sm.pick[3] = hist[dd]; }
   }
   __syncthreads();
   d = sm.pick[0];
@@ -221,6 +221,76 @@ __device__ void leader_finish(TopkSmem& sm, const uint2* cand, uint32_t n, uint3
   }
 }
 
+// Every CTA writes its keys > T (in position order, after the lower ranks') and its share
+// of the first need_eq keys == T (rank order is position order) to the output; returns the
+// cluster-wide count of keys > T.  Called by every thread of every CTA of the cluster.
+__device__ uint32_t cluster_write_selected(TopkSmem& sm, const uint32_t* keys, int c0, int len, uint32_t T,
+                                          uint32_t need_eq, int K, int32_t* out_idx, float* out_scores) {
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t nrank = cluster_nctarank();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  // counts of this CTA's keys above and at T, per warp, then per CTA through every rank
+  const int span = warp_span(len);
+  const int lo = warp * span, hi = min(len, lo + span);
+  uint32_t cg = 0, ce = 0;
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    const uint32_t k = i < hi ? keys[i] : 0u;
+    cg += __popc(__ballot_sync(0xffffffffu, k > T));
+    ce += __popc(__ballot_sync(0xffffffffu, k == T && k != 0u));
+  }
+  if (lane == 0) { sm.warp_cnt[0][warp] = cg; sm.warp_cnt[1][warp] = ce; }
+  __syncthreads();
+  if (tid < static_cast<int>(nrank)) {  // push this rank's counts into every rank's table
+    uint32_t my_gt = 0, my_eq = 0;
+    for (int w = 0; w < nw; ++w) { my_gt += sm.warp_cnt[0][w]; my_eq += sm.warp_cnt[1][w]; }
+    dsmem_st_u32(dsmem_addr(&sm.counts[0][rank], tid), my_gt);
+    dsmem_st_u32(dsmem_addr(&sm.counts[1][rank], tid), my_eq);
+  }
+  cluster_sync();
+  uint32_t gt_before = 0, eq_before = 0, gt_total = 0;
+  for (uint32_t r = 0; r < nrank; ++r) {
+    const uint32_t a = sm.counts[0][r], b = sm.counts[1][r];
+    if (r < rank) { gt_before += a; eq_before += b; }
+    gt_total += a;
+  }
+  const uint32_t eq_lo = eq_before < need_eq ? eq_before : need_eq;
+  const uint32_t eq_quota = need_eq - eq_lo;  // ties this CTA may still take
+
+  // ordered compaction of each warp's slice
+  uint32_t og = gt_before, oe = 0;
+  for (int w = 0; w < warp; ++w) { og += sm.warp_cnt[0][w]; oe += sm.warp_cnt[1][w]; }
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    const uint32_t k = i < hi ? keys[i] : 0u;
+    const uint32_t bg = __ballot_sync(0xffffffffu, k > T);
+    const uint32_t be = __ballot_sync(0xffffffffu, k == T && k != 0u);
+    if (k > T) {
+      const uint32_t slot = og + __popc(bg & lt);
+      if (slot < static_cast<uint32_t>(K)) {  // guards the row against an inconsistent count
+        out_idx[slot] = c0 + i;
+        if (out_scores) out_scores[slot] = key_score(k);
+      }
+    }
+    if (k == T && k != 0u) {
+      const uint32_t r = oe + __popc(be & lt);
+      if (r < eq_quota) {
+        const uint32_t slot = gt_total + eq_lo + r;
+        if (slot < static_cast<uint32_t>(K)) {
+          out_idx[slot] = c0 + i;
+          if (out_scores) out_scores[slot] = key_score(k);
+        }
+      }
+    }
+    og += __popc(bg);
+    oe += __popc(be);
+  }
+  // keep the counts alive until every rank has read them
+  cluster_sync();
+  return gt_total;
+}
+
 // Select the Top-K of one query row.
 //   keys[0..len)  this CTA's keys for positions c0 .. c0+len-1 (0 = not selectable);
 //                 16-byte aligned; chunk >= len is the chunk size of every CTA
@@ -269,8 +339,21 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, const uint3
   __syncthreads();
   uint32_t d0, above0;
   block_pick(sm, sm.hist[0], static_cast<uint32_t>(K), d0, above0);
+  const bool found = sm.pick[2] != 0;
   // every thread has read the picks; the copy is refilled only after a later cluster barrier
   for (int i = tid; i < kHistBins; i += nt) sm.hist[0][i] = 0;
+  if (!found) {
+    // fewer than K selectable keys although n_sel > K (positions on pages flagged bad):
+    // keep every selectable key, in position order, and pad the rest of the row with -1
+    const uint32_t n_valid = cluster_write_selected(sm, keys, c0, len, 0u, 0u, K, out_idx, out_scores);
+    if (rank == 0) {
+      for (int s = static_cast<int>(n_valid) + tid; s < K; s += nt) {
+        out_idx[s] = -1;
+        if (out_scores) out_scores[s] = -INFINITY;
+      }
+    }
+    return;
+  }
 
   const uint32_t at_total = sm.pick[3];  // cluster-wide count of keys in bin d0
   if (at_total <= static_cast<uint32_t>(cand_cap)) {
@@ -355,67 +438,7 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, const uint3
     need -= sm.bcast[1];
   }
   const uint32_t T = prefix;
-  const uint32_t need_eq = need;  // >= 1
-
-  // counts of this CTA's keys above and at T, per warp, then per CTA through every rank
-  const int span = warp_span(len);
-  const int lo = warp * span, hi = min(len, lo + span);
-  uint32_t cg = 0, ce = 0;
-  for (int base = lo; base < hi; base += 32) {
-    const int i = base + lane;
-    const uint32_t k = i < hi ? keys[i] : 0u;
-    cg += __popc(__ballot_sync(0xffffffffu, k > T));
-    ce += __popc(__ballot_sync(0xffffffffu, k == T && k != 0u));
-  }
-  if (lane == 0) { sm.warp_cnt[0][warp] = cg; sm.warp_cnt[1][warp] = ce; }
-  __syncthreads();
-  if (tid < static_cast<int>(nrank)) {  // push this rank's counts into every rank's table
-    uint32_t my_gt = 0, my_eq = 0;
-    for (int w = 0; w < nw; ++w) { my_gt += sm.warp_cnt[0][w]; my_eq += sm.warp_cnt[1][w]; }
-    dsmem_st_u32(dsmem_addr(&sm.counts[0][rank], tid), my_gt);
-    dsmem_st_u32(dsmem_addr(&sm.counts[1][rank], tid), my_eq);
-  }
-  cluster_sync();
-  uint32_t gt_before = 0, eq_before = 0, gt_total = 0;
-  for (uint32_t r = 0; r < nrank; ++r) {
-    const uint32_t a = sm.counts[0][r], b = sm.counts[1][r];
-    if (r < rank) { gt_before += a; eq_before += b; }
-    gt_total += a;
-  }
-  const uint32_t eq_lo = eq_before < need_eq ? eq_before : need_eq;
-  const uint32_t eq_quota = need_eq - eq_lo;  // ties this CTA may still take
-
-  // ordered compaction of each warp's slice
-  uint32_t og = gt_before, oe = 0;
-  for (int w = 0; w < warp; ++w) { og += sm.warp_cnt[0][w]; oe += sm.warp_cnt[1][w]; }
-  const uint32_t lt = (1u << lane) - 1u;
-  for (int base = lo; base < hi; base += 32) {
-    const int i = base + lane;
-    const uint32_t k = i < hi ? keys[i] : 0u;
-    const uint32_t bg = __ballot_sync(0xffffffffu, k > T);
-    const uint32_t be = __ballot_sync(0xffffffffu, k == T && k != 0u);
-    if (k > T) {
-      const uint32_t slot = og + __popc(bg & lt);
-      if (slot < static_cast<uint32_t>(K)) {  // guards the row against an inconsistent count
-        out_idx[slot] = c0 + i;
-        if (out_scores) out_scores[slot] = key_score(k);
-      }
-    }
-    if (k == T && k != 0u) {
-      const uint32_t r = oe + __popc(be & lt);
-      if (r < eq_quota) {
-        const uint32_t slot = gt_total + eq_lo + r;
-        if (slot < static_cast<uint32_t>(K)) {
-          out_idx[slot] = c0 + i;
-          if (out_scores) out_scores[slot] = key_score(k);
-        }
-      }
-    }
-    og += __popc(bg);
-    oe += __popc(be);
-  }
-  // keep the counts alive until every rank has read them
-  cluster_sync();
+  cluster_write_selected(sm, keys, c0, len, T, need, K, out_idx, out_scores);  // need >= 1 ties
 }
 
 }  // namespace dsa

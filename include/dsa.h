@@ -71,7 +71,8 @@ enum {
   DSA_STATUS_BAD_SEQ = 2,       /* q_seq outside [0, n_seq) or a group spans two sequences */
   DSA_STATUS_BAD_LEN = 4,       /* seq_len outside [0, max_ctx] */
   DSA_STATUS_BAD_INDEX = 8,     /* Top-K index outside the row's sequence */
-  DSA_STATUS_TIMEOUT = 16       /* a bounded wait inside a kernel gave up */
+  DSA_STATUS_TIMEOUT = 16,      /* a bounded wait inside a kernel gave up */
+  DSA_STATUS_NAN_SCORE = 32     /* an indexer score was NaN (ranked below every other score) */
 };
 
 /*
@@ -255,6 +256,20 @@ int dsa_sparse_attn_noalloc(const void* q_bf16, int32_t n_q, int32_t h_s, const 
  * it.  Returns a negative DSA_ERR_CUDA if the synchronisation itself failed.
  */
 int dsa_device_status(void* stream);
+
+/*
+ * dsa_test_stall_indexer -- a testing aid for the kernels' bounded waits; not for
+ * production use.  Every wait inside a kernel on an mbarrier gives up after a limit
+ * (about one second), sets DSA_STATUS_TIMEOUT and lets the kernel finish instead of
+ * hanging.  With wait_limit_us > 0, every indexer launch that follows in this process
+ * (dsa_indexer_topk, dsa_indexer_scores, dsa_decode_step) uses that limit, and its
+ * copy-issuing lanes stop before their first copy, as a stalled producer would.  The
+ * consumers' waits then run out: the kernel sets DSA_STATUS_TIMEOUT, skips the rest of its
+ * work, waits for its own copies and tensor-core products in flight, frees its tensor
+ * memory and returns; its rows come back as -1 (no position scored).  0 restores normal
+ * operation.  Returns DSA_ERR_INVALID_ARG outside 0..10000000.
+ */
+int dsa_test_stall_indexer(int32_t wait_limit_us);
 
 /* dsa_last_error -- message for the last non-zero return on this host thread. */
 const char* dsa_last_error(void);
