@@ -34,7 +34,7 @@ V_DIM = 512
 KCACHE_PAGE_BYTES = 8448
 KVCACHE_TOKEN_BYTES = 608
 
-STATUS_BITS = {1: "BAD_PAGE", 2: "BAD_SEQ", 4: "BAD_LEN", 8: "BAD_INDEX", 16: "TIMEOUT", 32: "NAN_SCORE"}
+STATUS_BITS = {1: "BAD_PAGE", 2: "BAD_SEQ", 4: "BAD_LEN", 8: "BAD_INDEX", 16: "TIMEOUT", 32: "NAN_SCORE", 64: "INTERNAL"}
 
 _lib = None
 

@@ -11,41 +11,38 @@
 // Absorbed MLA decode: each selected position j gives one dequantised latent row kv[j]
 // (576 wide); it is the key and kv[j][0:512] is the value.
 //
-// One CTA handles one query row and one contiguous share ("split") of its selected
-// entries, for all heads at once (M = 128 rows of the MMAs; rows >= h_s are zero).
-// Sixteen warps, each role in its own warps so that no role's latency sits in another's
-// loop:
-//   warps 0, 1  Q K^T of the even and the odd tiles: Q (bf16, 128 x 576, resident, loaded
-//               once by TMA) times a gathered tile (32 entries x 576) into one of two S
-//               buffers in TMEM, so the next tile's QK^T runs while the softmax works on this
-//               one.  Two issuing warps, because a single thread issues an MMA only every
-//               ~55 cycles while the operand reads of one take ~40.
-//   warps 4-7   S -> P, one head per thread: online softmax in the exp2 domain with a
-//               lazily updated running max (the accumulator is rescaled only when the max
-//               grows by more than 2^8), P written to shared memory as bf16.
-//   warps 8-11  the tail rounds, added into register accumulators (rescaled with the max
-//               that the S -> P warps publish per tile).
-//   lane 0 of warp 4 also issues every P V once the tile's P is stored: O[:, 0:448] into
-//               its TMEM accumulator, and O[:, 448:512] in two 32-column rounds through the
-//               tile's S buffer (free once its S was read).  The first round goes ahead of
-//               the large products, so the tail warps read it while those run; the second
-//               is issued at the start of the next tile, so the softmax never waits for it.
-//   warps 2, 3, 12-15  gather: index -> page -> record, 16-byte loads of E4M3 codes,
-//               multiply by the tile scale, bf16 into the 128-byte-swizzled operand tile
-//               (double buffered; the next tile's codes are loaded and converted in
-//               registers before its buffer is free).  Invalid entries (-1, or past the
-//               sequence) become zero rows.
-// TMEM (512 columns): O[:, 0:448] in columns 0..447, S buffers in 448..479 (even tiles)
-// and 480..511 (odd tiles).  At N = 32 an MMA costs ~40 cycles of the SM's operand reads
-// whatever issues it (a 4 KB Q slice and a 1 KB tile slice from shared memory), so QK^T's
-// 36 K-steps are the largest cost of a tile.  With two KV buffers next to the resident Q,
-// a buffer is refilled only after its tile's P V products, so the chain gather -> Q K^T ->
-// softmax -> P V -> tail rounds, once per two tiles, sets the pace (~4400 cycles a tile).
-// Several splits of a row write their partial outputs (each normalised by its own sum,
-// bf16) with their running max and sums to the workspace; a small kernel merges them
-// (log-sum-exp weights).  (Merging inside
-// a cluster of the row's splits, through distributed shared memory or through L2, measured
-// slower: the split-merge kernel runs spread over the whole GPU.)
+// One CTA handles one query row, one contiguous share ("split") of its selected entries
+// and one half of the 512 value columns, for all heads at once (M = 128 rows of the MMAs;
+// rows >= h_s are zero).  The two CTAs of a (row, split) compute the same logits and the
+// same weights (the same instructions on the same data), so each finishes its own half of
+// the output with no exchange.  Halving the output accumulator leaves tensor memory for
+// the query's first 384 dims, which then feed Q K^T straight from TMEM; only the last 192
+// dims are read from shared memory, and the room this frees holds four KV buffers, so the
+// gather runs up to three tiles ahead of the tensor cores.
+//
+// Twenty-three warps, each role in its own warps:
+//   warps 0, 1    Q K^T of the even / odd tiles (32 entries x 576) into their own S buffer
+//                 (24 K-steps with the query in TMEM, 12 with it in shared memory); warp 0
+//                 also loads the shared-memory part of Q (TMA).
+//   warps 4-11    S -> P for entries 0..15 (warps 4-7) and 16..31 (warps 8-11) of a tile,
+//                 one head per thread (TMEM lane quadrant = warp mod 4): the two warps of
+//                 a quadrant share each tile's maximum through shared memory, keep a
+//                 lazily updated running max (the accumulator is rescaled only when the
+//                 max grows by more than 2^8) and write P as bf16 over their own S columns.
+//                 At the start they store the query's TMEM part.
+//   warp 22       P V (A = P from TMEM, B = the tile's value half from shared memory); it
+//                 alone waits for each product and publishes how many have completed, which
+//                 the S -> P warps read only when they must rescale O.
+//   warps 2, 3, 12-21  gather: index -> page -> record, 16-byte loads of E4M3 codes, times
+//                 the tile scale, bf16 into the 128-byte-swizzled operand tile (four
+//                 buffers; the next tile's codes are converted in registers before its
+//                 buffer is free).  Invalid entries (-1, or past the sequence) become zero
+//                 rows.  Twelve warps, three on each SM sub-partition, so that the
+//                 conversion's instruction stream is spread evenly.
+// TMEM (512 columns): O (128 x 256 fp32) in 0..255, S buffers in 256..287 / 288..319 (P
+// over columns 0..7 and 16..23 of its buffer), Q dims 0..383 (bf16 pairs) in 320..511.
+// Several splits of a row write partial outputs (each normalised by its own sum, bf16)
+// with their running max and sums to the workspace; a small kernel merges them.
 
 #include <algorithm>
 #include <cfloat>
@@ -60,60 +57,68 @@ namespace dsa {
 namespace {
 
 constexpr int kTok = 32;                       // selected entries per tile
+constexpr int kHalfV = kVDim / 2;              // value columns per CTA
 constexpr int kWarpQK = 0;                     // warps 0, 1: Q K^T of the even / odd tiles (0: the Q load)
-constexpr int kWarpSoft0 = 4;                  // warps 4..7: S -> P, one TMEM lane quadrant each; warp 4 issues P V
-constexpr int kWarpTail0 = 8;                  // warps 8..11: tail rounds, one quadrant each
-constexpr int kGatherWarps = 6;                // warps 2, 3 and 12..15
-constexpr int kThreads = 512;
+constexpr int kWarpSoft0 = 4;                  // warps 4..11: S -> P
+constexpr int kWarpPV = 22;                    // warp 22: P V
+constexpr int kGatherWarps = 12;               // warps 2, 3 and 12..21
+constexpr int kThreads = 32 * 23;
+constexpr int kNumKv = 4;                      // KV buffers (tile j uses buffer j mod 4)
+constexpr int kQTmemSteps = 24;                // K-steps of Q K^T with Q in TMEM (dims 0..383)
 constexpr int kQBlock = 128 * 128;             // one 64-column K-block of Q: 128 rows x 128 B
-constexpr int kQBytes = 9 * kQBlock;           // 147456
+constexpr int kQSmemBlocks = 3;                // dims 384..575 in shared memory
+constexpr int kQBytes = kQSmemBlocks * kQBlock;  // 49152
 constexpr int kKvBlock = kTok * 128;           // one 64-column K-block of a tile: 4096 B
 constexpr int kKvBytes = 9 * kKvBlock;         // 36864
-constexpr int kPBytes = 128 * kTok * 2;        // 8192
-constexpr uint32_t kColS = 448;                // S buffers (tile j: kColS + 32 (j & 1)), tail rounds
-constexpr int kVLeft = 448;                    // output columns accumulated in TMEM
-constexpr int kVTail = 64;                     // output columns accumulated in registers
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;
 constexpr int kChunks = kLatent / 16;          // 16-byte code chunks per entry (36)
-constexpr int kSplitTarget = 148;              // CTAs the split count aims for
 constexpr int kMaxSplit = 16;
 constexpr float kRescaleLog2 = 8.0f;           // lazy max update threshold (factor 256)
 
-// Every barrier waited on by parity has waiters that cannot fall two phases behind: each
-// next phase needs something the waiters do after their wait.
 struct Ctl {
-  uint64_t q_full;
-  uint64_t kv_full[2];     // gather -> everyone: tile in buffer b
-  uint64_t kv_empty[2];    // QK^T and the P V products of the tile are done with buffer b
-  uint64_t s_full[2];      // S of the tile in S buffer b is ready
-  uint64_t s_free[2];      // S buffer b is free again (its tail rounds have been read)
-  uint64_t p_full;         // P of the tile is in shared memory
-  uint64_t p_free;         // every P V product of the tile has completed
-  uint64_t m_ready[2];     // the running max of the tile in S buffer b is in s_m[b]
-  uint64_t tail_full[2];   // a tail round is in S buffer b (two phases per tile)
-  uint64_t tail_empty;     // the first tail round has been read
+  uint64_t q_full;             // the shared-memory part of Q has landed (TMA)
+  uint64_t q_tmem;             // the TMEM part of Q is stored (8 softmax warps)
+  uint64_t kv_full[kNumKv];    // gather -> everyone: tile in buffer k
+  uint64_t kv_empty[kNumKv];   // the P V product of the tile in buffer k has completed
+  uint64_t s_full[2];          // S of the tile in S buffer b is ready
+  uint64_t s_free[2];          // the P in S buffer b has been consumed by its P V product
+  uint64_t p_full[2];          // P of the tile in S buffer b is in TMEM and O is rescaled (8 arrivals)
+  uint64_t p_done;             // the P V product of the tile has completed (the P V warp waits)
   uint32_t tmem_base;
   int abort;
-  uint8_t valid[2][kTok];  // per KV buffer: selected entry t of the tile is a real cache row
+  int pv_count;                // P V products known complete (written by the P V warp)
+  uint8_t valid[kNumKv][kTok]; // per KV buffer: selected entry t of the tile is a real cache row
 };
 
 constexpr uint32_t kOffQ = 0;
-constexpr int kStagePitch = kVDim * 2 + 16;    // staged bf16 output row (padded against bank conflicts)
-static_assert(128 * kStagePitch <= kQBytes, "the output rows are staged in the Q buffer");
 constexpr uint32_t kOffKv = kQBytes;
-constexpr uint32_t kOffP = kOffKv + 2 * kKvBytes;
-constexpr uint32_t kOffCtl = kOffP + kPBytes;
-constexpr uint32_t kCtlBytes = 256;
-constexpr uint32_t kOffM = kOffCtl + kCtlBytes;  // running max of each head, per tile parity
-constexpr uint32_t kMBytes = 2 * 128 * 4;
-constexpr uint32_t kSmemBytes = kOffM + kMBytes + 1024;  // + slack for the 1024-byte alignment
+constexpr uint32_t kOffCtl = kOffKv + kNumKv * kKvBytes;
+constexpr uint32_t kCtlBytes = 512;
+constexpr uint32_t kOffMx = kOffCtl + kCtlBytes;  // [2 tile parities][2 halves][128] tile maxima
+constexpr uint32_t kMxBytes = 2 * 2 * 128 * 4;
+// At the end the idle KV buffers hold the staged output rows and the final (max, sums).
+constexpr int kStagePitch = kHalfV * 2 + 16;   // staged bf16 output row (padded against bank conflicts)
+constexpr uint32_t kOffStage = kOffKv;
+constexpr uint32_t kOffFin = kOffKv + 2 * kKvBytes;
+static_assert(128 * kStagePitch <= 2 * kKvBytes, "the output rows are staged in KV buffers 0 and 1");
+// The dynamic shared memory starts 1024-byte aligned (it follows the block's reserved
+// 1 KB); the kernel checks this and refuses to run otherwise.
+constexpr uint32_t kSmemBytes = kOffMx + kMxBytes;
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
+static_assert(kSmemBytes <= 232448, "shared memory");
 
-__host__ __device__ inline int split_count(int n_q, int topk) {
+__host__ __device__ inline int split_count(int n_q, int topk, int n_sm) {
   const int tiles = (topk + kTok - 1) / kTok;
-  int s = kSplitTarget / (n_q > 0 ? n_q : 1);
+  int s = n_sm / (2 * (n_q > 0 ? n_q : 1));
   s = s < 1 ? 1 : s;
   s = s > kMaxSplit ? kMaxSplit : s;
   return s > tiles ? tiles : s;
+}
+
+int sm_count() {
+  DevInfo di;
+  const char* why = nullptr;
+  return device_info(&di, &why) ? di.n_sm : 152;
 }
 
 struct SfaPlan {
@@ -135,36 +140,110 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// D (+)= A * B with bf16 operands and fp32 accumulation, issued by one elected lane of a
+// converged warp (every lane executes the instruction stream; only the elected one
+// issues: a converged warp issues MMAs at a steadier rate than a single active lane).
+// The _ts form takes A (M = 128 rows, K = 16 bf16 per row as 8 packed columns) from TMEM.
+__device__ __forceinline__ void mma_bf16_ts_el(uint32_t d, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                               bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+      :: "r"(d), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+      : "memory");
+}
+__device__ __forceinline__ void mma_bf16_ss_el(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+      :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+      : "memory");
+}
+// tcgen05.commit from the elected lane of a converged warp (the lane that issued the MMAs)
+__device__ __forceinline__ void commit_el(uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}"
+      :: "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" :: "r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+// Wait until at least n P V products are known complete (bounded like the mbarrier waits).
+__device__ __forceinline__ bool wait_pv_count(const int* cnt, int n, volatile int* abort, unsigned* status) {
+  if (ld_acquire(cnt) >= n) return true;
+  const uint64_t t0 = tc::global_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (ld_acquire(cnt) >= n) return true;
+    if ((it & 255u) == 255u) {
+      if (*abort) return false;
+      if (tc::global_ns() - t0 > tc::kWaitLimitNs) {
+        *abort = 1;
+        flag(status, DSA_STATUS_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+         "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+         "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
-  extern __shared__ uint8_t smem_dyn[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* s_q = smem + kOffQ;
   uint8_t* s_kv = smem + kOffKv;
-  uint8_t* s_p = smem + kOffP;
   Ctl& ctl = *reinterpret_cast<Ctl*>(smem + kOffCtl);
-  float* s_m = reinterpret_cast<float*>(smem + kOffM);  // [2][128]
+  float* s_mx = reinterpret_cast<float*>(smem + kOffMx);  // [2][2][128]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x, t = blockIdx.y;
+  const int split = blockIdx.x >> 1, half = blockIdx.x & 1, t = blockIdx.y;
   const int tile0 = split * pl.tiles_total / pl.nsplit;
   const int nt = (split + 1) * pl.tiles_total / pl.nsplit - tile0;
+  // every swizzled operand tile needs 1024-byte alignment (uniform over the block)
+  if (smem_u32(smem) & 1023u) {
+    if (tid == 0) flag(a.status, DSA_STATUS_INTERNAL);
+    return;
+  }
 
   if (tid == 0) {
     ctl.abort = 0;
     tc::mbar_init(&ctl.q_full, 1);
-    for (int b = 0; b < 2; ++b) {
-      tc::mbar_init(&ctl.kv_full[b], kGatherWarps);
-      tc::mbar_init(&ctl.kv_empty[b], 2);
-      tc::mbar_init(&ctl.s_full[b], 1);
-      tc::mbar_init(&ctl.s_free[b], 4);
-      tc::mbar_init(&ctl.tail_full[b], 1);
+    tc::mbar_init(&ctl.q_tmem, 8);
+    for (int k = 0; k < kNumKv; ++k) {
+      tc::mbar_init(&ctl.kv_full[k], kGatherWarps);
+      tc::mbar_init(&ctl.kv_empty[k], 1);
     }
-    tc::mbar_init(&ctl.p_full, 4);
-    tc::mbar_init(&ctl.p_free, 1);
-    tc::mbar_init(&ctl.m_ready[0], 4);
-    tc::mbar_init(&ctl.m_ready[1], 4);
-    tc::mbar_init(&ctl.tail_empty, 4);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&ctl.s_full[b], 1);
+      tc::mbar_init(&ctl.s_free[b], 1);
+    }
+    tc::mbar_init(&ctl.p_full[0], 8);
+    tc::mbar_init(&ctl.p_full[1], 8);
+    tc::mbar_init(&ctl.p_done, 1);
+    ctl.pv_count = 0;
     tc::mbar_fence_init();
   }
   if (warp == 0) tc::tmem_alloc(&ctl.tmem_base, 512);
@@ -181,132 +260,113 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
   const int L = seq_ok ? a.seq_lens[seq] : 0;
   const int32_t* ptab = a.page_table + static_cast<size_t>(seq_ok ? seq : 0) * a.max_pages;
   const int32_t* idx = a.idx + static_cast<size_t>(t) * a.topk;
-  if (tid == 0 && !seq_ok && split == 0) flag(a.status, DSA_STATUS_BAD_SEQ);
-
-  // P V of tile j, issued by one thread: O[:, 0:448] into the TMEM accumulator, and
-  // O[:, 448:512] in two 32-column rounds through S buffer j & 1 (its S has been read) that
-  // the tail warps add into registers.  The second round waits until the tail warps have
-  // read the first, so its issue is deferred to the start of the next tile (pv_second_round),
-  // and the issuing thread goes on with the softmax meanwhile.
-  const uint32_t id_v0 = tc::idesc_bf16(256, false, true);
-  const uint32_t id_v1 = tc::idesc_bf16(192, false, true);
-  const uint32_t id_vt = tc::idesc_bf16(kTok, false, true);
-  auto pv_desc = [&](int j, int ks, uint64_t& pd, uint64_t& vd) {
-    pd = tc::smem_desc(smem_u32(s_p + ks * 256), 128, 512, 0);
-    vd = tc::smem_desc(smem_u32(s_kv + (j & 1) * kKvBytes + ks * 2048), kKvBlock, 1024, 2);  // 16 entries = two 8-row groups
-  };
-  auto pv_main = [&](int j) {
-    const int b = j & 1;
-    tc::mbar_wait(&ctl.p_full, j & 1, abort, a.status);  // every S -> P warp has stored its rows
-    tc::fence_after_sync();
-    // the first tail round goes first: the tail warps read it while the large products run
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {  // columns 448.. : 7 K-blocks into the tile
-      uint64_t pd, vd;
-      pv_desc(j, ks, pd, vd);
-      tc::mma_bf16(tmem + kColS + kTok * b, pd, vd + 7 * (kKvBlock >> 4), id_vt, ks > 0);
-    }
-    tc::commit(&ctl.tail_full[b]);
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-      uint64_t pd, vd;
-      pv_desc(j, ks, pd, vd);
-      tc::mma_bf16(tmem + 0, pd, vd, id_v0, j > 0 || ks > 0);
-      tc::mma_bf16(tmem + 256, pd, vd + 4 * (kKvBlock >> 4), id_v1, j > 0 || ks > 0);
-    }
-  };
-  auto pv_second_round = [&](int j) {
-    const int b = j & 1;
-    tc::mbar_wait(&ctl.tail_empty, j & 1, abort, a.status);  // every tail warp has read round one
-    tc::fence_after_sync();
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {  // columns 480.. : 64 bytes further into the swizzle atom
-      uint64_t pd, vd;
-      pv_desc(j, ks, pd, vd);
-      tc::mma_bf16(tmem + kColS + kTok * b, pd, vd + (7 * (kKvBlock >> 4) + 4), id_vt, ks > 0);
-    }
-    tc::commit(&ctl.tail_full[b]);
-    tc::commit(&ctl.kv_empty[b]);
-    tc::commit(&ctl.p_free);
-  };
+  if (tid == 0 && !seq_ok && split == 0 && half == 0) flag(a.status, DSA_STATUS_BAD_SEQ);
 
   if (warp == kWarpQK || warp == kWarpQK + 1) {
     // ---------------- Q K^T issuers ----------------
-    // warp kWarpQK + b issues the tiles j = b (mod 2), from lane 0: one thread issues an MMA
-    // only every ~55 cycles and two lanes of one warp take turns, while two warps keep the
-    // tensor core's operand reads busy.  Each warp owns one S buffer and one KV buffer, so
-    // every barrier it waits on keeps a single waiter and its operands stay fixed.
+    // warp kWarpQK + b issues the tiles j = b (mod 2) from lane 0 into S buffer b; they sit
+    // in KV buffers b and b + 2 in turn, so the loop takes them two at a time and every
+    // operand address stays fixed.  Two issuing warps, because one thread issues an MMA
+    // only every ~45 cycles.
     const int b = warp - kWarpQK;
-    if (lane == 0) {
-      if (b == 0) {
-        tc::prefetch_tmap(&qmap);
-        tc::mbar_arrive_expect_tx(&ctl.q_full, kQBytes);
-        for (int kb = 0; kb < 9; ++kb) tc::tma_load_3d(s_q + kb * kQBlock, &qmap, kb * 64, 0, t, &ctl.q_full);
-      }
-      const uint32_t id_qk = tc::idesc_bf16(kTok, false, false);
-      tc::mbar_wait(&ctl.q_full, 0, abort, a.status);
-      // descriptors advance by adding (byte offset >> 4) to the start-address field
-      const uint64_t qd0 = tc::desc_kmajor_sw128(smem_u32(s_q));
-      const uint64_t kd = tc::desc_kmajor_sw128(smem_u32(s_kv + b * kKvBytes));
-      const uint32_t d = tmem + kColS + kTok * b;
-      for (int j = b; j < nt; j += 2) {
-        // S = Q K^T of tile j into S buffer b
-        tc::mbar_wait(&ctl.kv_full[b], (j >> 1) & 1, abort, a.status);
-        tc::mbar_wait(&ctl.s_free[b], ((j >> 1) & 1) ^ 1, abort, a.status);
-        tc::fence_after_sync();
-#pragma unroll
-        for (int st = 0; st < 36; ++st) {
-          const uint32_t kb = st >> 2, k = st & 3;
-          tc::mma_bf16(d, qd0 + (kb * (kQBlock >> 4) + 2 * k), kd + (kb * (kKvBlock >> 4) + 2 * k), id_qk, st > 0);
-        }
-        tc::commit(&ctl.s_full[b]);
-        tc::commit(&ctl.kv_empty[b]);
-      }
+    if (b == 0 && lane == 0) {
+      tc::prefetch_tmap(&qmap);
+      tc::mbar_arrive_expect_tx(&ctl.q_full, kQBytes);
+      for (int kb = 0; kb < kQSmemBlocks; ++kb)
+        tc::tma_load_3d(s_q + kb * kQBlock, &qmap, kQTmemSteps * 16 + kb * 64, 0, t, &ctl.q_full);
     }
     __syncwarp();
-  } else if (warp >= kWarpSoft0 && warp < kWarpSoft0 + 4) {
-    // ---------------- S -> P (warps 4..7) ----------------
+    const uint32_t id_qk = tc::idesc_bf16(kTok, false, false);
+    tc::mbar_wait(&ctl.q_full, 0, abort, a.status);
+    tc::mbar_wait(&ctl.q_tmem, 0, abort, a.status);
+    // descriptors advance by adding (byte offset >> 4) to the start-address field
+    const uint64_t qd = tc::desc_kmajor_sw128(smem_u32(s_q));
+    const uint32_t d = tmem + kColS + kTok * b;
+    auto qk = [&](int j, uint64_t kd) {
+      tc::mbar_wait(&ctl.kv_full[j & 3], (j >> 2) & 1, abort, a.status);
+      tc::mbar_wait(&ctl.s_free[b], ((j >> 1) & 1) ^ 1, abort, a.status);
+      __syncwarp();
+      tc::fence_after_sync();
+#pragma unroll
+      for (int st = 0; st < kQTmemSteps; ++st)  // dims 16 st .. : Q from TMEM
+        mma_bf16_ts_el(d, tmem + kColQ + 8 * st, kd + ((st >> 2) * (kKvBlock >> 4) + 2 * (st & 3)), id_qk, st > 0);
+#pragma unroll
+      for (int st = kQTmemSteps; st < 36; ++st) {  // dims 384.. : Q from shared memory
+        const int qs = st - kQTmemSteps;
+        mma_bf16_ss_el(d, qd + ((qs >> 2) * (kQBlock >> 4) + 2 * (qs & 3)),
+                       kd + ((st >> 2) * (kKvBlock >> 4) + 2 * (st & 3)), id_qk, true);
+      }
+      commit_el(&ctl.s_full[b]);
+    };
+    const uint64_t kd0 = tc::desc_kmajor_sw128(smem_u32(s_kv + b * kKvBytes));
+    const uint64_t kd1 = tc::desc_kmajor_sw128(smem_u32(s_kv + (b + 2) * kKvBytes));
+    for (int j = b; j < nt; j += 4) {
+      qk(j, kd0);
+      if (j + 2 < nt) qk(j + 2, kd1);
+    }
+    __syncwarp();
+  } else if (warp >= kWarpSoft0 && warp < kWarpSoft0 + 8) {
+    // ---------------- S -> P (warps 4..11) ----------------
     const int quarter = warp & 3;
-    const int m = quarter * 32 + lane;  // head row
+    const int hv = (warp - kWarpSoft0) >> 2;  // entries 16 hv .. 16 hv + 15 of every tile
+    const int m = quarter * 32 + lane;        // head row
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    // the query's first 384 dims into TMEM (dims 192 hv .. +191 of head m, bf16 pairs)
+    {
+      uint32_t r[32];
+#pragma unroll
+      for (int h3 = 0; h3 < 3; ++h3) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
+                                                          (static_cast<size_t>(t) * a.h_s + m) * kLatent +
+                                                          192 * hv + 64 * h3);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (m < a.h_s) v = __ldg(src + i);
+          r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_base + kColQ + 96 * hv + 32 * h3, r);
+      }
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&ctl.q_tmem);
+    }
     const float c2 = a.sm_scale * 1.4426950408889634f;  // logits in log2 units
     // l sums the bf16-rounded weights that the P V product uses (it normalises O);
     // lx sums the unrounded weights (it gives the log-sum-exp)
     float m_ref = -INFINITY, l = 0.f, lx = 0.f;
-    // lane 0 of warp 4 issues every P V (see pv_main, pv_second_round)
-    const bool pv = warp == kWarpSoft0 && lane == 0;
+    const uint32_t bar_pair = 1 + quarter;            // named barrier of the quadrant's two warps
     for (int j = 0; j < nt; ++j) {
-      const int b = j & 1;
-      if (pv && j > 0) pv_second_round(j - 1);
-      __syncwarp();
+      const int b = j & 1, kb = j & 3;
       // the gather warps flag the tile's real entries before they release the buffer
-      tc::mbar_wait(&ctl.kv_full[b], (j >> 1) & 1, abort, a.status);
-      const uint32_t mask = __ballot_sync(0xffffffffu, ctl.valid[b][lane] != 0);
+      tc::mbar_wait(&ctl.kv_full[kb], (j >> 2) & 1, abort, a.status);
+      const uint32_t mask = __ballot_sync(0xffffffffu, lane < 16 && ctl.valid[kb][16 * hv + (lane & 15)] != 0);
       tc::mbar_wait(&ctl.s_full[b], (j >> 1) & 1, abort, a.status);
       tc::fence_after_sync();
-      uint32_t sr[32];
-      tc::tmem_ld32(tmem + lane_base + kColS + kTok * b, sr);
+      const uint32_t sb = tmem + lane_base + kColS + kTok * b + 16 * hv;
+      uint32_t sr[16];
+      tc::tmem_ld16(sb, sr);
       tc::tmem_wait_ld();
-      float x[32];
+      float x[16];
       float mt = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 16; ++i) {
         x[i] = ((mask >> i) & 1u) ? __uint_as_float(sr[i]) * c2 : -INFINITY;
         mt = fmaxf(mt, x[i]);
       }
+      // the tile's maximum over both halves (slot by tile parity: the partner reads slot
+      // j & 1 before it passes the barrier of tile j + 1, after which it is rewritten)
+      s_mx[((j & 1) * 2 + hv) * 128 + m] = mt;
+      asm volatile("bar.sync %0, 64;" :: "r"(bar_pair) : "memory");
+      mt = fmaxf(mt, s_mx[((j & 1) * 2 + (hv ^ 1)) * 128 + m]);
       const bool need = mt > m_ref + kRescaleLog2 || (m_ref == -INFINITY && mt > -INFINITY);
       const float m_new = need ? mt : m_ref;
       const float alpha = need ? fast_exp2(m_ref - m_new) : 1.f;  // 2^-inf = 0
-      // the tail warps rescale their part of the accumulator with the same max
-      s_m[b * 128 + m] = m_new;
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&ctl.m_ready[b]);
-      // the weights need only the new max: they are formed while the previous tile's
-      // products may still be running
-      uint32_t pk[16];
+      uint32_t pk[8];
       float lsum = 0.f, lxsum = 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
+      for (int i = 0; i < 16; i += 2) {
         const float p0 = (m_new == -INFINITY) ? 0.f : fast_exp2(x[i] - m_new);
         const float p1 = (m_new == -INFINITY) ? 0.f : fast_exp2(x[i + 1] - m_new);
         const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
@@ -314,109 +374,81 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
         lxsum += p0 + p1;
         pk[i >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
       }
-      // every P V product of the previous tile has completed: P may be overwritten and the
-      // TMEM accumulator rescaled
-      if (j > 0) tc::mbar_wait(&ctl.p_free, (j - 1) & 1, abort, a.status);
-      tc::fence_after_sync();
+      // P over this warp's own (already read) S columns
+      tmem_st8(sb, pk);
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        for (int c = 0; c < kVLeft; c += 16) {
+        // O is rescaled once the previous tile's P V product has completed
+        wait_pv_count(&ctl.pv_count, j, abort, a.status);
+        tc::fence_after_sync();
+        // this warp's half of O's columns
+        for (int c = 128 * hv; c < 128 * hv + 128; c += 16) {
           uint32_t r[16];
-          tc::tmem_ld16(tmem + lane_base + c, r);
+          tc::tmem_ld16(tmem + lane_base + kColO + c, r);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tc::tmem_st16(tmem + lane_base + c, r);
+          tc::tmem_st16(tmem + lane_base + kColO + c, r);
         }
-        tc::tmem_wait_st();
       }
+      tc::tmem_wait_st();
       l = l * alpha + lsum;
       lx = lx * alpha + lxsum;
       m_ref = m_new;
-      // P row m: core matrix (m/8, chunk c) at (m/8)*512 + c*128, row offset (m%8)*16
-      uint8_t* prow = s_p + (m >> 3) * 512 + (m & 7) * 16;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(prow + c * 128) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      tc::fence_async_smem();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&ctl.p_full);
-      if (pv) pv_main(j);
-      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&ctl.p_full[b]);
     }
-    if (pv && nt > 0) pv_second_round(nt - 1);
-    __syncwarp();
-    // every product has completed; hand (max, sums) to the tail warps through the P buffer
-    if (nt > 0) tc::mbar_wait(&ctl.p_free, (nt - 1) & 1, abort, a.status);
+    // every product has completed; publish (max, sums) for the output phase
+    wait_pv_count(&ctl.pv_count, nt, abort, a.status);
     tc::fence_after_sync();
-    float* s_fin = reinterpret_cast<float*>(s_p);  // [3][128]
-    s_fin[m] = m_ref;
-    s_fin[128 + m] = l;
-    s_fin[256 + m] = lx;
-    asm volatile("bar.sync 1, 256;" ::: "memory");  // S -> P and tail warps
-    // (the TMEM columns are written by every warp after the role loops; see below)
-  } else if (warp >= kWarpTail0 && warp < kWarpTail0 + 4) {
-    // ---------------- tail rounds (warps 8..11): output columns 448..511 ----------------
-    const int quarter = warp & 3;
-    const int m = quarter * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    float m_prev = -INFINITY;
-    float ot[kVTail];
-#pragma unroll
-    for (int i = 0; i < kVTail; ++i) ot[i] = 0.f;
+    float* s_fin = reinterpret_cast<float*>(smem + kOffFin);  // [0]: max; [1 + hv]: l; [3 + hv]: lx
+    if (hv == 0) s_fin[m] = m_ref;
+    s_fin[(1 + hv) * 128 + m] = l;
+    s_fin[(3 + hv) * 128 + m] = lx;
+  } else if (warp == kWarpPV) {
+    // ---------------- P V (warp 22) ----------------
+    // O += P V over each tile's 32 entries (2 K-steps of 16): A = P from S buffer b (entries
+    // 0..15 in its columns 0..7, 16..31 in 16..23), B = this CTA's value half of the tile
+    // (MN-major: 64-column blocks 4096 bytes apart, 8-entry groups 1024 bytes apart).  This
+    // warp is the only waiter of p_done and waits for every product in turn, so its parity
+    // never falls behind; the products chain through O, so waiting costs only the gap
+    // before the next issue.
+    const uint32_t id_pv = tc::idesc_bf16(kHalfV, false, true);
     for (int j = 0; j < nt; ++j) {
-      const int b = j & 1;
-      // the running max the S -> P warps used for this tile: rescale by the same factor
-      tc::mbar_wait(&ctl.m_ready[b], (j >> 1) & 1, abort, a.status);
-      const float m_new = s_m[b * 128 + m];
-      const float alpha = (m_new == m_prev) ? 1.f : fast_exp2(m_prev - m_new);  // 2^-inf = 0
-      m_prev = m_new;
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      const int b = j & 1, kb = j & 3;
+      // (one barrier per S buffer: the S -> P warps reach tile j + 2 only after this
+      // product has freed the buffer, so the waiter never falls two phases behind)
+      tc::mbar_wait(&ctl.p_full[b], (j >> 1) & 1, abort, a.status);
+      __syncwarp();
+      tc::fence_after_sync();
+      const uint32_t pbase = tmem + kColS + kTok * b;
+      const uint32_t vaddr = smem_u32(s_kv + kb * kKvBytes + 4 * half * kKvBlock);
 #pragma unroll
-        for (int i = 0; i < kVTail; ++i) ot[i] *= alpha;
+      for (int ks = 0; ks < 2; ++ks) {
+        const uint64_t vd = tc::smem_desc(vaddr + ks * 2048, kKvBlock, 1024, 2);
+        mma_bf16_ts_el(tmem + kColO, pbase + 16 * ks, vd, id_pv, j > 0 || ks > 0);
       }
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        tc::mbar_wait(&ctl.tail_full[b], r, abort, a.status);
-        tc::fence_after_sync();
-        uint32_t rr[32];
-        tc::tmem_ld32(tmem + lane_base + kColS + kTok * b, rr);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) ot[32 * r + i] += __uint_as_float(rr[i]);
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(r == 0 ? &ctl.tail_empty : &ctl.s_free[b]);
-      }
+      commit_el(&ctl.s_free[b]);
+      commit_el(&ctl.kv_empty[kb]);
+      commit_el(&ctl.p_done);
+      tc::mbar_wait(&ctl.p_done, j & 1, abort, a.status);
+      tc::fence_after_sync();
+      __syncwarp();
+      if (lane == 0) st_release(&ctl.pv_count, j + 1);
     }
-    asm volatile("bar.sync 1, 256;" ::: "memory");  // (max, sums) from the S -> P warps
-    const float* s_fin = reinterpret_cast<const float*>(s_p);
-    const float m_ref = s_fin[m], l = s_fin[128 + m], lx = s_fin[256 + m];
-    // columns 448..511 into the staged output rows (written out below by every warp)
-    {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint8_t* row = smem + kOffQ + m * kStagePitch + 2 * kVLeft;
-#pragma unroll
-      for (int c = 0; c < kVTail; c += 8)
-        *reinterpret_cast<uint4*>(row + 2 * c) =
-            make_uint4(pack_bf16(ot[c] * inv, ot[c + 1] * inv), pack_bf16(ot[c + 2] * inv, ot[c + 3] * inv),
-                       pack_bf16(ot[c + 4] * inv, ot[c + 5] * inv), pack_bf16(ot[c + 6] * inv, ot[c + 7] * inv));
-    }
-    (void)m_ref;
-    (void)lx;
   } else {
-    // ---------------- gather + dequantise (warps 2, 3, 12..15) ----------------
-    // Thread g owns entry tok = g / 6 of every tile and its 16-byte code chunks
-    // c = s, s + 6, .., s + 30 (s = g % 6): one index -> page -> record lookup per tile, and
-    // six threads read one record's 576 codes in contiguous 96-byte runs.  The loads run
-    // ahead of their use: while tile j is converted, the index entry of tile j + 4, the page
-    // of tile j + 3, an L2 prefetch of the records of tile j + 2 and the codes of tile j + 1
-    // are in flight, so no iteration waits on a load it issued itself and the code loads
-    // find their lines in L2.
-    static_assert(kTok * 6 == 32 * kGatherWarps && kChunks == 36, "six threads per entry, six chunks each");
-    const int g = (warp < 4 ? warp - 2 : warp - 10) * 32 + lane;  // 0..191
-    const int tok = g / 6, s6 = g % 6;
-    const bool reporter = s6 == 0;              // one thread per entry reports bad input
+    // ---------------- gather + dequantise (warps 2, 3, 12..21) ----------------
+    // Thread g owns entry tok = g / 12 of every tile and its 16-byte code chunks
+    // c = s, s + 12, s + 24 (s = g % 12): one index -> page -> record lookup per tile, and
+    // twelve threads read one record's 576 codes in contiguous 192-byte runs.  The loads
+    // run ahead of their use: while tile j is converted, the index entry of tile j + 4, the
+    // page of tile j + 3, an L2 prefetch of the records of tile j + 2 and the codes of tile
+    // j + 1 are in flight, so no iteration waits on a load it issued itself.
+    constexpr int kPer = 3;  // chunks per thread
+    static_assert(kTok * 12 == 32 * kGatherWarps && kChunks == 12 * kPer, "twelve threads per entry");
+    const int g = (warp < 4 ? warp - 2 : warp - 10) * 32 + lane;  // 0..383
+    const int tok = g / 12, s12 = g % 12;
+    const bool reporter = s12 == 0;             // one thread per entry reports bad input
     auto ld_s32 = [](const int32_t* ptr) {
       int v;
       asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(ptr));
@@ -430,8 +462,8 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     auto in_range = [&](int p) { return p >= 0 && p < L && p / kPage < a.max_pages; };
     // physical page of position p (-1 when p is out of range)
     auto page_of = [&](int p) -> int { return in_range(p) ? ld_s32(ptab + p / kPage) : -1; };
-    uint4 code[6];
-    float scl[6];
+    uint4 code[kPer];
+    float scl[kPer];
     bool live = false;
     // request the codes of the entry at position p on page pg
     auto load_codes = [&](int p, int pg) {
@@ -447,15 +479,15 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
         }
       }
 #pragma unroll
-      for (int k = 0; k < 6; ++k) {
+      for (int k = 0; k < kPer; ++k) {
         code[k] = make_uint4(0u, 0u, 0u, 0u);
         scl[k] = 0.f;
       }
       if (rec) {
         live = true;
 #pragma unroll
-        for (int k = 0; k < 6; ++k) {
-          const int c = s6 + 6 * k;
+        for (int k = 0; k < kPer; ++k) {
+          const int c = s12 + 12 * k;
           asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(code[k].x), "=r"(code[k].y), "=r"(code[k].z), "=r"(code[k].w)
                        : "l"(rec + 16 * c));
@@ -464,12 +496,12 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
         }
       }
     };
-    // pull the record of the entry at position p on page pg towards L2 (the six threads of
-    // the entry take one 128-byte line each; together they cover the 608-byte record)
+    // pull the 608-byte record of the entry at position p on page pg towards L2 (five of
+    // the entry's twelve threads take one 128-byte line each)
     auto prefetch_record = [&](int p, int pg) {
-      if (in_range(p) && pg >= 0 && pg < a.num_pages) {
+      if (s12 < 5 && in_range(p) && pg >= 0 && pg < a.num_pages) {
         const uint8_t* rec = a.kv_cache + (static_cast<int64_t>(pg) * kPage + p % kPage) * kKvTokBytes;
-        asm volatile("prefetch.global.L2 [%0];" :: "l"(rec + min(128 * s6, kKvTokBytes - 1)));
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(rec + min(128 * s12, kKvTokBytes - 1)));
       }
     };
     // warm L2 with this split's index entries and the sequence's page-table row (one
@@ -477,7 +509,8 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     {
       const int e_lo = tile0 * kTok, e_hi = min(a.topk, (tile0 + nt) * kTok);
       const int npg = min(a.max_pages, (L + kPage - 1) / kPage);
-      if (e_lo + 32 * g < e_hi) asm volatile("prefetch.global.L2 [%0];" :: "l"(idx + e_lo + 32 * g));
+      for (int e = e_lo + 32 * g; e < e_hi; e += 32 * 32 * kGatherWarps)
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(idx + e));
       for (int i = 32 * g; i < npg; i += 32 * 32 * kGatherWarps)
         asm volatile("prefetch.global.L2 [%0];" :: "l"(ptab + i));
     }
@@ -489,18 +522,18 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
     load_codes(p1, pg1);
     p1 = p2; pg1 = pg2; p2 = p3; pg2 = pg3; p3 = p4;
     for (int j = 0; j < nt; ++j) {
-      const int b = j & 1;
-      uint8_t* kv = s_kv + b * kKvBytes;
+      const int kb = j & 3;
+      uint8_t* kv = s_kv + kb * kKvBytes;
       // requests for the tiles ahead: the index of j + 4, the page of j + 3 and the record of
       // j + 2 (towards L2) now, the codes of j + 1 once this tile's have left their registers
       const int p4n = entry(j + 4);
       const int pg3n = page_of(p3);
       prefetch_record(p2, pg2);
       // this tile's codes -> bf16 in registers
-      uint4 o0s[6], o1s[6];
+      uint4 o0s[kPer], o1s[kPer];
       const bool live_j = live;
 #pragma unroll
-      for (int k = 0; k < 6; ++k) {
+      for (int k = 0; k < kPer; ++k) {
         const uint32_t w[4] = {code[k].x, code[k].y, code[k].z, code[k].w};
         uint32_t o[8];
 #pragma unroll
@@ -519,61 +552,58 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
       }
       load_codes(p1, pg1);
       p1 = p2; pg1 = pg2; p2 = p3; pg2 = pg3n; p3 = p4n;
-      tc::mbar_wait(&ctl.kv_empty[b], ((j >> 1) & 1) ^ 1, abort, a.status);
+      tc::mbar_wait(&ctl.kv_empty[kb], ((j >> 2) & 1) ^ 1, abort, a.status);
 #pragma unroll
-      for (int k = 0; k < 6; ++k) {
-        const int c = s6 + 6 * k;
-        const int kb = c >> 2, cc = (c & 3) * 2;
-        uint8_t* row = kv + kb * kKvBlock + tok * 128;
+      for (int k = 0; k < kPer; ++k) {
+        const int c = s12 + 12 * k;
+        const int kblk = c >> 2, cc = (c & 3) * 2;
+        uint8_t* row = kv + kblk * kKvBlock + tok * 128;
         *reinterpret_cast<uint4*>(row + ((cc ^ (tok & 7)) << 4)) = o0s[k];
         *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (tok & 7)) << 4)) = o1s[k];
       }
-      if (reporter) ctl.valid[b][tok] = live_j ? 1 : 0;
+      if (reporter) ctl.valid[kb][tok] = live_j ? 1 : 0;
       tc::fence_async_smem();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&ctl.kv_full[b]);
+      if (lane == 0) tc::mbar_arrive(&ctl.kv_full[kb]);
     }
   }
   // ---- the output rows, normalised, as bf16: to the output (one split) or to the
-  // workspace (several splits; merged by sfa_combine_kernel).  Columns 0..447 come from
-  // TMEM: warp w reads its lane quadrant (w mod 4), columns 112 (w / 4) .. +112, and stages
-  // them in the (idle) Q buffer next to the tail warps' columns; then every warp writes
-  // whole rows, 512 contiguous bytes per instruction. ----
+  // workspace (several splits; merged by sfa_combine_kernel).  Warp w reads its lane
+  // quadrant (w mod 4), columns 64 (w / 4) .. +64, and stages them in the idle KV buffers;
+  // then every warp writes whole rows, 512 contiguous bytes per instruction. ----
   tc::fence_before_sync();
   __syncthreads();  // the S -> P warps have seen the last product complete and published (m, l, lx)
   tc::fence_after_sync();
+  uint8_t* s_stage = smem + kOffStage;
   {
-    const float* s_fin = reinterpret_cast<const float*>(s_p);  // [3][128]: max, l, lx
+    const float* s_fin = reinterpret_cast<const float*>(smem + kOffFin);
     const int quarter = warp & 3;
     const int m = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const float l = s_fin[128 + m];
+    const float l = s_fin[128 + m] + s_fin[256 + m];
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    uint8_t* row = smem + kOffQ + m * kStagePitch;
-    const int cbeg = 112 * (warp >> 2);
-    for (int c = cbeg; c < cbeg + 112; c += 32) {
+    uint8_t* row = s_stage + m * kStagePitch;
+    const int cbeg = 64 * (warp >> 2);
+#pragma unroll
+    for (int c = cbeg; c < cbeg + 64 && warp < 16; c += 32) {
       uint32_t r[32];
-      const int nc = min(32, cbeg + 112 - c);  // 32, 32, 32, 16
       if (nt > 0) {
-        tc::tmem_ld16(tmem + lane_base + c, reinterpret_cast<uint32_t(&)[16]>(r[0]));
-        if (nc > 16) tc::tmem_ld16(tmem + lane_base + c + 16, reinterpret_cast<uint32_t(&)[16]>(r[16]));
+        tc::tmem_ld32(tmem + lane_base + kColO + c, r);
         tc::tmem_wait_ld();
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) r[i] = 0u;
       }
 #pragma unroll
-      for (int i = 0; i < 32; i += 8) {
-        if (i < nc)
-          *reinterpret_cast<uint4*>(row + 2 * (c + i)) =
-              make_uint4(pack_bf16(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv),
-                         pack_bf16(__uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv),
-                         pack_bf16(__uint_as_float(r[i + 4]) * inv, __uint_as_float(r[i + 5]) * inv),
-                         pack_bf16(__uint_as_float(r[i + 6]) * inv, __uint_as_float(r[i + 7]) * inv));
-      }
+      for (int i = 0; i < 32; i += 8)
+        *reinterpret_cast<uint4*>(row + 2 * (c + i)) =
+            make_uint4(pack_bf16(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv),
+                       pack_bf16(__uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv),
+                       pack_bf16(__uint_as_float(r[i + 4]) * inv, __uint_as_float(r[i + 5]) * inv),
+                       pack_bf16(__uint_as_float(r[i + 6]) * inv, __uint_as_float(r[i + 7]) * inv));
     }
-    if (m < a.h_s && warp >= kWarpSoft0 && warp < kWarpSoft0 + 4) {
-      const float m_ref = s_fin[m], lx = s_fin[256 + m];
+    if (half == 0 && m < a.h_s && warp >= kWarpSoft0 && warp < kWarpSoft0 + 4) {
+      const float m_ref = s_fin[m], lx = s_fin[384 + m] + s_fin[512 + m];
       const size_t slot = (static_cast<size_t>(t) * pl.nsplit + split) * a.h_s + m;
       if (pl.nsplit == 1) {
         if (a.out_lse)
@@ -585,14 +615,14 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
   }
   __syncthreads();  // every staged row is complete
   {
-    // row h: 64 pieces of 16 bytes; thread i takes piece i % 64 of rows i / 64, + 8, ..
-    const int piece = tid & 63;
-    for (int h = tid >> 6; h < a.h_s; h += kThreads / 64) {
+    // row h: 32 pieces of 16 bytes; warp w writes rows w, w + 23, ..
+    const int piece = tid & 31;
+    for (int h = tid >> 5; h < a.h_s; h += kThreads / 32) {
       __nv_bfloat16* dst = pl.nsplit == 1
                                ? static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(t) * a.h_s + h) * kVDim
                                : pl.ws_o + ((static_cast<size_t>(t) * pl.nsplit + split) * a.h_s + h) * kVDim;
-      *reinterpret_cast<uint4*>(dst + 8 * piece) =
-          *reinterpret_cast<const uint4*>(smem + kOffQ + h * kStagePitch + 16 * piece);
+      *reinterpret_cast<uint4*>(dst + kHalfV * half + 8 * piece) =
+          *reinterpret_cast<const uint4*>(s_stage + h * kStagePitch + 16 * piece);
     }
   }
   tc::fence_before_sync();
@@ -658,7 +688,7 @@ size_t ws_o_bytes(int n_q, int h_s, int ns) {
 }  // namespace
 
 size_t sfa_workspace_bytes(int n_q, int h_s, int topk) {
-  const int ns = split_count(n_q, topk);
+  const int ns = split_count(n_q, topk, sm_count());
   if (ns <= 1) return 0;
   return ws_o_bytes(n_q, h_s, ns) + static_cast<size_t>(n_q) * ns * h_s * 4 * sizeof(float);
 }
@@ -666,7 +696,7 @@ size_t sfa_workspace_bytes(int n_q, int h_s, int topk) {
 cudaError_t launch_sfa(const SfaArgs& a, cudaStream_t s, const char** err) {
   if (a.n_q == 0) return cudaSuccess;
   SfaPlan pl{};
-  pl.nsplit = split_count(a.n_q, a.topk);
+  pl.nsplit = split_count(a.n_q, a.topk, sm_count());
   pl.tiles_total = (a.topk + kTok - 1) / kTok;
   if (pl.nsplit > 1) {
     pl.ws_o = static_cast<__nv_bfloat16*>(a.workspace);
@@ -693,7 +723,7 @@ cudaError_t launch_sfa(const SfaArgs& a, cudaStream_t s, const char** err) {
   cudaError_t e = cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  e = launch_pdl(sfa_tc_kernel, dim3(pl.nsplit, a.n_q), dim3(kThreads), kSmemBytes, s, 1, qmap, a, pl);
+  e = launch_pdl(sfa_tc_kernel, dim3(2 * pl.nsplit, a.n_q), dim3(kThreads), kSmemBytes, s, 1, qmap, a, pl);
   if (e != cudaSuccess || pl.nsplit == 1) return e;
   return launch_pdl(sfa_combine_kernel, dim3(a.n_q, a.h_s), dim3(128), 0, s, 1, a, pl);
 }

@@ -72,7 +72,8 @@ enum {
   DSA_STATUS_BAD_LEN = 4,       /* seq_len outside [0, max_ctx] */
   DSA_STATUS_BAD_INDEX = 8,     /* Top-K index outside the row's sequence */
   DSA_STATUS_TIMEOUT = 16,      /* a bounded wait inside a kernel gave up */
-  DSA_STATUS_NAN_SCORE = 32     /* an indexer score was NaN (ranked below every other score) */
+  DSA_STATUS_NAN_SCORE = 32,    /* an indexer score was NaN (ranked below every other score) */
+  DSA_STATUS_INTERNAL = 64      /* a kernel found its shared memory misaligned and did nothing */
 };
 
 /*
