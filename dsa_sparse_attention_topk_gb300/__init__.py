@@ -71,6 +71,8 @@ _SIGS = {
                                        _P]),
     "dsa_device_status": (ctypes.c_int, [_P]),
     "dsa_test_stall_indexer": (ctypes.c_int, [_I32]),
+    "dsa_topk_merge": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P]),
+    "dsa_lse_combine": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P]),
     "dsa_last_error": (ctypes.c_char_p, []),
     "dsa_version": (ctypes.c_int, []),
 }
@@ -260,6 +262,44 @@ def sparse_attn_noalloc(q, kv_cache, page_table, seq_lens, q_seq, topk_idx, sm_s
 
 
 NOALLOC_SCRATCH_BYTES = 40 * 1024 * 1024
+
+
+def topk_merge(cand_idx, cand_scores, topk, part_offsets=None, local_lo=None, local_hi=None, out_idx=None,
+               out_scores=None, stream=None):
+    """The K highest of several parts' candidates per row (context parallelism).
+    cand_idx int32 / cand_scores fp32 [n_parts, n_q, k_in] (part-local positions, -1 empty);
+    part_offsets int32 [n_parts, n_q] or None.  Returns (out_idx int32 [n_q, topk] global
+    positions by score then position, out_scores fp32, out_local int32 [n_q, topk] or None:
+    the positions inside [local_lo, local_hi) relative to local_lo, -1 elsewhere)."""
+    _need(cand_idx, torch.int32, "cand_idx")
+    _need(cand_scores, torch.float32, "cand_scores")
+    n_parts, n_q, k_in = cand_idx.shape
+    if out_idx is None:
+        out_idx = torch.empty(n_q, topk, dtype=torch.int32, device=cand_idx.device)
+    if out_scores is None:
+        out_scores = torch.empty(n_q, topk, dtype=torch.float32, device=cand_idx.device)
+    out_local = None
+    if local_lo is not None:
+        out_local = torch.empty(n_q, topk, dtype=torch.int32, device=cand_idx.device)
+    _check(lib().dsa_topk_merge(_ptr(cand_idx), _ptr(cand_scores), _ptr(part_offsets), n_parts, n_q, k_in, topk,
+                                _ptr(out_idx), _ptr(out_scores), _ptr(local_lo), _ptr(local_hi), _ptr(out_local),
+                                _stream(stream)))
+    return out_idx, out_scores, out_local
+
+
+def lse_combine(o_parts, lse_parts, out=None, out_lse=None, stream=None):
+    """Combine attention outputs over disjoint entry sets: o_parts bf16 [n_parts, n_q, h, 512],
+    lse_parts fp32 [n_parts, n_q, h].  Returns (out bf16 [n_q, h, 512], out_lse fp32)."""
+    _need(o_parts, torch.bfloat16, "o_parts")
+    _need(lse_parts, torch.float32, "lse_parts")
+    n_parts, n_q, h, _ = o_parts.shape
+    if out is None:
+        out = torch.empty(n_q, h, V_DIM, dtype=torch.bfloat16, device=o_parts.device)
+    if out_lse is None:
+        out_lse = torch.empty(n_q, h, dtype=torch.float32, device=o_parts.device)
+    _check(lib().dsa_lse_combine(_ptr(o_parts), _ptr(lse_parts), n_parts, n_q, h, _ptr(out), _ptr(out_lse),
+                                 _stream(stream)))
+    return out, out_lse
 
 
 def device_status(stream=None):

@@ -94,7 +94,7 @@ bool dsa::device_info(DevInfo* out, const char** err) {
 
 extern "C" {
 
-int dsa_version(void) { return 100; }
+int dsa_version(void) { return 101; }
 
 const char* dsa_last_error(void) { return t_last_error.c_str(); }
 
@@ -332,6 +332,39 @@ int dsa_sparse_attn_noalloc(const void* q_bf16, int32_t n_q, int32_t h_s, const 
   if (e != cudaSuccess)
     return why ? fail(DSA_ERR_UNSUPPORTED, "%s", why) : cuda_fail(e, "sparse_attn_noalloc launch");
   return DSA_OK;
+}
+
+int dsa_topk_merge(const int32_t* cand_idx, const float* cand_scores, const int32_t* part_offsets, int32_t n_parts,
+                   int32_t n_q, int32_t k_in, int32_t topk, int32_t* out_idx, float* out_scores,
+                   const int32_t* local_lo, const int32_t* local_hi, int32_t* out_local, void* stream) {
+  if (n_q < 0) return fail(DSA_ERR_INVALID_ARG, "topk_merge: n_q < 0");
+  if (n_parts < 1 || k_in < 1 || topk < 1) return fail(DSA_ERR_INVALID_ARG, "topk_merge: n_parts, k_in and topk must be >= 1");
+  if (static_cast<int64_t>(n_parts) * k_in > 16384)
+    return fail(DSA_ERR_UNSUPPORTED, "topk_merge: n_parts * k_in must be <= 16384 (got %lld)",
+                static_cast<long long>(n_parts) * k_in);
+  if (n_q == 0) return DSA_OK;
+  if (!cand_idx || !cand_scores || !out_idx) return fail(DSA_ERR_INVALID_ARG, "topk_merge: null pointer");
+  if ((out_local != nullptr) != (local_lo != nullptr && local_hi != nullptr))
+    return fail(DSA_ERR_INVALID_ARG, "topk_merge: out_local needs local_lo and local_hi (and they need it)");
+  unsigned* st = status_ptr();
+  if (!st) return fail(DSA_ERR_CUDA, "topk_merge: no CUDA device");
+  dsa::TopkMergeArgs a{cand_idx, cand_scores, part_offsets, n_parts, n_q, k_in, topk, out_idx, out_scores,
+                       local_lo, local_hi, out_local, st};
+  cudaError_t e = dsa::launch_topk_merge(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSA_OK : cuda_fail(e, "topk_merge launch");
+}
+
+int dsa_lse_combine(const void* o_parts, const float* lse_parts, int32_t n_parts, int32_t n_q, int32_t h,
+                    void* out_bf16, float* out_lse, void* stream) {
+  if (n_q < 0) return fail(DSA_ERR_INVALID_ARG, "lse_combine: n_q < 0");
+  if (n_parts < 1 || h < 1 || h > 65535) return fail(DSA_ERR_INVALID_ARG, "lse_combine: n_parts >= 1 and h in 1..65535");
+  if (n_q == 0) return DSA_OK;
+  if (!o_parts || !lse_parts || !out_bf16) return fail(DSA_ERR_INVALID_ARG, "lse_combine: null pointer");
+  if (!aligned(o_parts, 8) || !aligned(out_bf16, 8))
+    return fail(DSA_ERR_INVALID_ARG, "lse_combine: o_parts and out must be 8-byte aligned");
+  cudaError_t e = dsa::launch_lse_combine(o_parts, lse_parts, n_parts, n_q, h, out_bf16, out_lse,
+                                          static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSA_OK : cuda_fail(e, "lse_combine launch");
 }
 
 int dsa_test_stall_indexer(int32_t wait_limit_us) {

@@ -90,6 +90,23 @@ struct SfaArgs {
   unsigned* status;
 };
 
+struct TopkMergeArgs {
+  const int32_t* cand_idx;      // [n_parts][n_q][k_in] part-local positions, -1 = empty
+  const float* cand_scores;     // same layout
+  const int32_t* part_offsets;  // [n_parts][n_q] added to a part's positions, or null (0)
+  int n_parts, n_q, k_in, topk;
+  int32_t* out_idx;             // [n_q][topk]
+  float* out_scores;            // [n_q][topk] or null
+  const int32_t* local_lo;      // [n_q] or null: with local_hi, the range out_local keeps
+  const int32_t* local_hi;
+  int32_t* out_local;           // [n_q][topk] or null: out_idx - local_lo inside the range, else -1
+  unsigned* status;
+};
+int topk_merge_pow2(int n);
+cudaError_t launch_topk_merge(const TopkMergeArgs& a, cudaStream_t s);
+cudaError_t launch_lse_combine(const void* o_parts, const float* lse_parts, int n_parts, int n_q, int h, void* out,
+                               float* out_lse, cudaStream_t s);
+
 // Each returns cudaSuccess or the launch error; `err` gets a short reason for
 // configuration problems detected while planning the launch.
 cudaError_t launch_quant_mxfp8(const void* k, const int64_t* slots, int n_tokens, uint8_t* cache,

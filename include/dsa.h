@@ -28,6 +28,11 @@
  *   position p of sequence b lives in physical page page_table[b * max_pages + p / 64],
  *   row p % 64; its cache "slot" is page * 64 + p % 64.
  * - Positions are logical positions inside the sequence (0-based).
+ * - Per device, the library looks up the device addresses of its own device-side words
+ *   (the status word, the scratch array of dsa_sparse_attn_noalloc) and queries the
+ *   multiprocessor count once, then keeps them for the life of the process.  A call
+ *   after cudaDeviceReset (or any teardown of the device's primary context) would use
+ *   stale addresses: the library must not outlive a reset of a device it has used.
  *
  * Cache layouts (bytes)
  * ---------------------
@@ -257,6 +262,52 @@ int dsa_sparse_attn_noalloc(const void* q_bf16, int32_t n_q, int32_t h_s, const 
  * it.  Returns a negative DSA_ERR_CUDA if the synchronisation itself failed.
  */
 int dsa_device_status(void* stream);
+
+/*
+ * Context parallelism.  "Deep Dive into Sparse Attention ..." section 3 and "Adapting and
+ * Optimizing Kimi K3.1 Pro for Long-Sequence Inference" section 4 shard the context of a
+ * long sequence over devices.  Each device runs dsa_indexer_topk on its shard (a
+ * page-aligned range of positions [lo, hi), seen as a sequence of its own: the page-table
+ * slice, seq_len hi - lo, q_pos - lo), keeping its local Top-K with scores; the devices
+ * exchange those candidates once; dsa_topk_merge turns them into the global Top-K; each
+ * device runs dsa_sparse_attn over the selected entries in its shard; the devices
+ * exchange (o, lse) once more; dsa_lse_combine gives the output.  Both exchanges are the
+ * caller's (for instance an all-gather); the result equals the single-device path.
+ */
+
+/*
+ * dsa_topk_merge -- the K highest of several parts' candidates, per query row.
+ *   cand_idx      [n_parts][n_q][k_in] int32 part-local positions, -1 = empty.
+ *   cand_scores   [n_parts][n_q][k_in] fp32 their scores.
+ *   part_offsets  nullable [n_parts][n_q] int32 added to part p's positions of row t
+ *                 (a shard's first position); null means 0.
+ *   topk          K.  n_parts * k_in <= 16384.
+ *   out_idx       [n_q][topk] int32 global positions ordered by score (highest first),
+ *                 equal scores by lower position; -1 after the last real candidate.
+ *   out_scores    nullable [n_q][topk] fp32 their scores (-inf where out_idx is -1).
+ *   local_lo, local_hi, out_local   all null, or all given: [n_q] int32 bounds of this
+ *                 device's shard and [n_q][topk] int32 out_idx - local_lo where out_idx lies
+ *                 in [local_lo, local_hi), else -1 (the selected entries this device holds,
+ *                 as positions of its shard, ready for dsa_sparse_attn).
+ * NaN scores rank below every other score.  A merged position outside int32 flags
+ * DSA_STATUS_BAD_INDEX and is dropped.
+ */
+int dsa_topk_merge(const int32_t* cand_idx, const float* cand_scores, const int32_t* part_offsets, int32_t n_parts,
+                   int32_t n_q, int32_t k_in, int32_t topk, int32_t* out_idx, float* out_scores,
+                   const int32_t* local_lo, const int32_t* local_hi, int32_t* out_local, void* stream);
+
+/*
+ * dsa_lse_combine -- combine attention outputs over disjoint sets of entries.
+ *   o_parts    [n_parts][n_q][h][512] bfloat16, each part normalised over its own entries
+ *              (as dsa_sparse_attn writes it), 8-byte aligned.
+ *   lse_parts  [n_parts][n_q][h] fp32 each part's log-sum-exp (natural log; -inf = the part
+ *              had no entry).
+ *   out_bf16   [n_q][h][512] bfloat16: sum_p exp(lse_p - L) o_p, L = log sum_p exp(lse_p).
+ *   out_lse    nullable [n_q][h] fp32 L.
+ * The softmax over a union of disjoint sets is this weighting of the softmaxes over the sets.
+ */
+int dsa_lse_combine(const void* o_parts, const float* lse_parts, int32_t n_parts, int32_t n_q, int32_t h,
+                    void* out_bf16, float* out_lse, void* stream);
 
 /*
  * dsa_test_stall_indexer -- a testing aid for the kernels' bounded waits; not for

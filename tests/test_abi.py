@@ -41,7 +41,7 @@ def test_binding_covers_every_declared_symbol(dsa):
 
 
 def test_version(dsa):
-    assert dsa.lib().dsa_version() == 100
+    assert dsa.lib().dsa_version() == 101
 
 
 def _idx_call(lib, **kw):

@@ -45,7 +45,7 @@ def _compare(ref, ref_lse, out, lse):
 
 
 def test_noalloc_matches_workspace_entry_point_two_calls_in_a_row(dsa):
-    # three query rows: each row is split over 16 CTAs, so the scratch array is used
+    # three query rows: each row is split over several CTAs, so the scratch array is used
     wl = W.custom([3000, 1500, 700], h_i=16, h_s=128, topk=512, seed=41)
     assert dsa.sparse_attn_workspace_size(wl.n_q, wl.h_s, wl.topk) > 0
     dw = DeviceWorkload(wl)
@@ -62,3 +62,16 @@ def test_noalloc_after_a_call_of_another_shape(dsa):
         dw = DeviceWorkload(wl)
         idx, _ = dw.indexer_topk(with_scores=False)
         _compare(*_both(dsa, dw, idx))
+
+
+def test_noalloc_at_the_largest_split_layout(dsa):
+    # nine rows of 2048 selected entries with 128 heads: the split count is as large as the
+    # GPU allows for nine rows, and the workspace it needs must fit the fixed array
+    wl = W.custom([2600 + 97 * i for i in range(9)], h_i=16, h_s=128, topk=2048, seed=44)
+    need = dsa.sparse_attn_workspace_size(wl.n_q, wl.h_s, wl.topk)
+    assert 0 < need <= dsa.NOALLOC_SCRATCH_BYTES
+    dw = DeviceWorkload(wl)
+    idx, _ = dw.indexer_topk(with_scores=False)
+    ref, ref_lse, out, lse = _both(dsa, dw, idx)
+    # the same kernels with the same split plan: equal bit for bit
+    assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
