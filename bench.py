@@ -206,7 +206,10 @@ def run_ours(args, rank, world, local_rank):
         dsa.sparse_attn(d["q_sfa"], layer.kv_cache, d["page_table"], d["seq_lens"], d["q_seq"], idx,
                         wl.sm_scale, out=out, out_lse=lse, workspace=ws)
 
-    launches_per_step = 3 + (1 if ws_n else 0)
+    # the step writes its new tokens inside the indexer (one per query row), then SFA and,
+    # with several splits, the split merge
+    fused = d["k_new"].shape[0] == n_q
+    launches_per_step = (0 if fused else 1) + 2 + (1 if ws_n else 0)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     for _ in range(max(3, args.warmup)):
         flush.zero_()

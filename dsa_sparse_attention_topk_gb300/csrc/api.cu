@@ -282,13 +282,28 @@ int dsa_decode_step(const void* k_new_bf16, const void* kv_new_bf16, const int64
   unsigned* st = status_ptr();
   if (!st) return fail(DSA_ERR_CUDA, "decode_step: no CUDA device");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = dsa::launch_quant_both(k_new_bf16, kv_new_bf16, slot_mapping, n_new, k_cache, kv_cache,
-                                         num_pages * DSA_PAGE_SIZE, st, s);
-  if (e != cudaSuccess) return cuda_fail(e, "decode_step: cache writer launch");
+  // one new token per query row (token i is row i's own token): the indexer writes them
+  // itself, each before it loads the page that holds it; otherwise a writer launch first
+  const bool fuse = n_new > 0 && n_new == n_q;
+  cudaError_t e = cudaSuccess;
+  if (!fuse) {
+    e = dsa::launch_quant_both(k_new_bf16, kv_new_bf16, slot_mapping, n_new, k_cache, kv_cache,
+                               num_pages * DSA_PAGE_SIZE, st, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode_step: cache writer launch");
+  }
   if (n_q == 0) return DSA_OK;
   dsa::IndexerArgs ia{q_idx_bf16, w, n_q, h_i, q_group, k_cache, num_pages, page_table, max_pages,
                       seq_lens, q_seq, q_pos, n_seq, max_ctx, topk, out_idx, nullptr, nullptr, st};
-  ia.early_inputs = n_new > 0 ? 1 : 0;  // the writer launched just above precedes the indexer
+  if (fuse) {
+    ia.fuse_writes = 1;
+    ia.k_new = k_new_bf16;
+    ia.kv_new = kv_new_bf16;
+    ia.slot_mapping = slot_mapping;
+    ia.kv_cache = kv_cache;
+    ia.num_slots = num_pages * DSA_PAGE_SIZE;
+  } else {
+    ia.early_inputs = n_new > 0 ? 1 : 0;  // the writer launched just above precedes the indexer
+  }
   apply_test_hooks(ia);
   const char* why = nullptr;
   e = dsa::launch_indexer(ia, s, &why);

@@ -64,6 +64,15 @@ struct IndexerArgs {
   // dependents only after its own wait; everything but the K-cache is then complete when
   // the indexer starts, and only the K-cache copies wait for the writer
   int early_inputs = 0;
+  // a decode step's new tokens, written by the indexer itself (fuse_writes = 1): token i is
+  // query row i's own token (its slot is row i's position in its sequence); its MXFP8 key
+  // goes to k_cache and its latent row to kv_cache, both at slot_mapping[i]
+  int fuse_writes = 0;
+  const void* k_new = nullptr;       // bf16 [n_q][128]
+  const void* kv_new = nullptr;      // bf16 [n_q][576]
+  const int64_t* slot_mapping = nullptr;
+  uint8_t* kv_cache = nullptr;
+  int64_t num_slots = 0;
   // testing aid for the bounded waits (dsa_test_stall_indexer): the waits' limit, and 1 to
   // make the copy-issuing lanes stop before their first copy
   uint64_t wait_ns = 1000000000ull;

@@ -34,6 +34,7 @@
 
 #include "dsa_common.cuh"
 #include "dsa_launch.h"
+#include "quant_tok.cuh"
 #include "tc_utils.cuh"
 #include "topk_cluster.cuh"
 
@@ -50,7 +51,10 @@ constexpr int kMaxAcc = 2;
 // moves between issuers and the ring has an even number of stages.
 __host__ __device__ constexpr int acc_count(int np) { return np <= 128 ? 2 : 1; }
 __host__ __device__ constexpr int mma_warps(int np) { return acc_count(np); }
-__host__ __device__ constexpr int threads_for(int np) { return 32 * (1 + mma_warps(np) + 4 * acc_count(np)); }
+// warps: the producer, the MMA issuers, the epilogue sets, and one warp that writes a decode
+// step's new tokens (fused writes) and otherwise only helps with the query quantisation
+__host__ __device__ constexpr int threads_for(int np) { return 32 * (2 + mma_warps(np) + 4 * acc_count(np)); }
+__host__ __device__ constexpr int writer_warp(int np) { return 1 + mma_warps(np) + 4 * acc_count(np); }
 constexpr int kTileP = 128;            // positions per MMA tile = two pages
 constexpr int kStageA = kTileP * kIdxDim;        // 16384 B of E4M3 codes
 constexpr int kStageSF = kTileP * 4;             // 512 B of E8M0 scales (position order)
@@ -76,11 +80,14 @@ struct Barriers {
   uint64_t tfull[kMaxAcc];
   uint64_t tempty[kMaxAcc];
   uint64_t drain[kMaxAcc];  // after an abort: the issuer's own MMAs have completed
+  uint64_t tok_written;     // this CTA's new tokens are in the K-cache (fused writes)
   uint32_t tmem_base;
   int abort;
   int seq;
   int n_max;
   int n_sel[4];
+  int tok_mine;             // bit j: this CTA writes row j's new token
+  int tok_tile;             // the first of its tiles that holds one of them (or a large value)
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -188,6 +195,27 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
     bs.seq = seq;
     bs.n_max = n_max;
     bs.abort = 0;
+    // fused writes: row j's new token (at its own position) is written by the CTA whose
+    // chunk holds that position, before the tile that holds it is loaded; a token outside
+    // every chunk (its row selects nothing there) goes to the last CTA
+    int mine = 0, tok_tile = 1 << 30;
+    if (a.fuse_writes) {
+      int chk = (n_max + C - 1) / C;
+      chk = (chk + kTileP - 1) / kTileP * kTileP;
+      if (chk > pl.chunk_cap) chk = pl.chunk_cap;
+      for (int j = 0; j < G; ++j) {
+        const int p = __ldcg(a.q_pos + row0 + j);
+        const bool scanned = p >= 0 && p < n_max && chk > 0;
+        const int owner = scanned ? min(p / chk, C - 1) : C - 1;
+        if (owner == rank) {
+          mine |= 1 << j;
+          if (scanned) tok_tile = min(tok_tile, (p - rank * chk) / kTileP);
+        }
+      }
+    }
+    bs.tok_mine = mine;
+    bs.tok_tile = tok_tile;
+    tc::mbar_init(&bs.tok_written, static_cast<uint32_t>(max(1, __popc(mine))));
     if (bad && rank == 0) flag(a.status, bad);
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(&bs.full[s], 1);
@@ -254,6 +282,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
       for (int t = a.stall_producer ? ntiles : lane; t < ntiles; t += kProd) {
         const int s = t % S, it = t / S;
         if (!tc::mbar_wait(&bs.empty[s], (it & 1) ^ 1, abort, a.status, wait_ns)) break;
+        // a tile holding this CTA's new token is loaded only after the token is written
+        if (t >= bs.tok_tile && !tc::mbar_wait(&bs.tok_written, 0, abort, a.status, wait_ns)) break;
         uint8_t* st = smem + pl.off_stage + s * kStageBytes;
         const int pg0 = s_pages[2 * t], pg1 = s_pages[2 * t + 1];
         if (pg0 == -2 || pg1 == -2) flag(a.status, DSA_STATUS_BAD_PAGE);
@@ -374,6 +404,30 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
       tc::mbar_drain(&bs.drain[mi], 0, wait_ns);
     }
     __syncwarp();
+  } else if (warp == writer_warp(Np)) {
+    // ---------------- fused writes: this CTA's share of the step's new tokens ----------------
+    // row e's token, if this CTA owns it, with the same quantisers as the writer kernels;
+    // the stores are made visible to the copy engine before the producer is signalled
+    for (int e = 0; e < G; ++e) {
+      if ((bs.tok_mine >> e) & 1) {
+        const int64_t i = row0 + e;
+        if (lane == 0 && seq >= 0) {
+          // the contract: token i sits at row i's own position (its scan sees it)
+          const int p = __ldcg(a.q_pos + i);
+          const int64_t own = (p >= 0 && p / kPage < a.max_pages)
+                                  ? static_cast<int64_t>(__ldcg(ptab + p / kPage)) * kPage + p % kPage
+                                  : -1;
+          if (own != __ldcg(a.slot_mapping + i)) flag(a.status, DSA_STATUS_BAD_PAGE);
+        }
+        const KTok kt = load_k_token(static_cast<const __nv_bfloat16*>(a.k_new), a.slot_mapping, i);
+        const KvTok vt = load_kv_token(static_cast<const __nv_bfloat16*>(a.kv_new), a.slot_mapping, i);
+        store_k_token(kt, const_cast<uint8_t*>(a.k_cache), a.num_slots, a.status);
+        store_kv_token(vt, a.kv_cache, a.num_slots, a.status);
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bs.tok_written);
+      }
+    }
   } else if (warp > kMma) {
     // ---------------- epilogue: set i (four warps) drains accumulator i ----------------
     const int set = (warp - 1 - kMma) >> 2;    // which accumulator this warp drains

@@ -59,10 +59,10 @@ class DsaDecodeLayer:
     def step(self, k_new, kv_new, slots_new, q_idx, w, q_sfa, page_table, seq_lens, q_seq, q_pos,
              max_ctx, q_group=1):
         """Write this step's tokens into both caches, then decode: one library call
-        (dsa_decode_step), which launches the cache writer, the indexer and SFA on the
-        current stream with programmatic dependent launch, so each kernel's set-up overlaps
-        the end of the one before, and the indexer reads its other inputs while the writer
-        runs.
+        (dsa_decode_step).  With one new token per query row the indexer kernel writes the
+        tokens itself, each before it loads the page that holds it, and SFA follows it on
+        the current stream with programmatic dependent launch; otherwise a writer kernel
+        runs first and the indexer reads its other inputs while the writer runs.
         """
         n_q = q_idx.shape[0]
         b = self._buffers(n_q)

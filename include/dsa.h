@@ -210,11 +210,17 @@ int dsa_sparse_attn(const void* q_bf16, int32_t n_q, int32_t h_s, const uint8_t*
  * dsa_decode_step -- one decode step of a DSA layer in one call: dsa_quant_kv for the
  * step's new tokens, then dsa_indexer_topk, then dsa_sparse_attn over its out_idx, on
  * `stream`, with the results each of those calls gives.  The pages describe the two
- * stages and the cache writes, not this packaging.  Because the library launches the
- * three kernels itself, it knows that the cache writer precedes the indexer: the indexer
- * then reads its queries, weights, sequence information and page table while the writer
- * is still running, and only its K-cache copies wait for the writer (a separate
- * dsa_indexer_topk call cannot assume that).
+ * stages and the cache writes ("Kimi K3.1 Pro Inference Acceleration ...", section
+ * "Lightning Indexer Three-Stream Coordination": the cache write runs alongside the
+ * indexer prolog), not this packaging.
+ *   When n_new == n_q, new token i must be query row i's own token: slot_mapping[i] is
+ *   the slot of position q_pos[i] of sequence q_seq[i] (a decode step's usual case).  The
+ *   indexer kernel then writes the tokens itself -- each in the CTA that scans its page,
+ *   before it loads that page -- and no writer kernel runs.  A slot_mapping[i] that is not
+ *   row i's own slot flags DSA_STATUS_BAD_PAGE (the token is still written there).
+ *   Otherwise the writer kernel runs first; the indexer reads its queries, weights,
+ *   sequence information and page table while the writer is still running, and only its
+ *   K-cache copies wait for the writer.
  *   k_new_bf16, kv_new_bf16, slot_mapping, n_new   as for dsa_quant_kv (n_new may be 0:
  *                        nothing is written, and the indexer waits as usual).
  *   k_cache, kv_cache    both caches, num_pages pages each (slots 0 .. 64 num_pages - 1).
