@@ -183,15 +183,53 @@ def check_topk(gpu_idx, gpu_vals, ref_s, mag, k):
 
 
 def lse_bound(q_row, kv_hat, idx, sm_scale):
-    """Per-head bound on |lse_gpu - lse_ref|.  The tensor-core path rounds each
-    dequantised latent value to bf16 (relative error <= 2^-9), so every logit moves by at
-    most sm_scale * sum_d |q_d kv_d| * 2^-9, and the log-sum-exp (a weighted mean of the
-    logits' moves) by at most the largest of those; fp32 summation adds a little."""
+    """Per-head worst-case bound on |lse_gpu - lse_ref| against the float64 oracle.  The
+    attention runs on the BF16 path ("Kimi K3.1 Pro Inference Acceleration ...", section
+    "Preserving a Mixed-Precision Path": BF16 for the final attention weighting), so each
+    dequantised latent value is rounded once to bf16 (relative error <= 2^-9): every logit
+    moves by at most sm_scale * sum_d |q_d kv_d| * 2^-9, and the log-sum-exp (a weighted
+    mean of the logits' moves) by at most the largest of those."""
     sel = np.asarray(idx)[np.asarray(idx) >= 0]
     if sel.size == 0:
         return np.zeros(q_row.shape[0])
     mag = np.abs(q_row) @ np.abs(kv_hat[sel]).T          # (H, J)
     return sm_scale * mag.max(axis=1) * 2.0 ** -9 + 1e-4
+
+
+# |lse_gpu - lse of the same attention over the bf16-rounded latent rows|: what is left is
+# fp32 accumulation of exact bf16 products over 576 terms and the hardware exp2 (relative
+# error ~2^-22).  Observed <= 5e-6 on every SFA case and on sampled full-size rows of all
+# four benchmark workloads; the gate keeps a 20x margin.
+LSE_BF16_ATOL = 1e-4
+
+
+def bf16_round(x):
+    """float64 -> float32 -> bfloat16 (round to nearest even) -> float64, as a float32
+    value computed by the kernel (an E4M3 code times its fp32 scale, exact in float64 and
+    correctly rounded to float32) is rounded to bf16."""
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).double().numpy()
+
+
+def check_lse(gpu_lse, q_row, kv_hat, idx, sm_scale, lse_ref):
+    """The row's lse against the float64 oracle (worst-case bound of the bf16 rounding) and
+    against the oracle over the bf16-rounded latent rows (LSE_BF16_ATOL).  Returns the two
+    largest deviations."""
+    idx = np.asarray(idx)
+    fin = np.isfinite(lse_ref)
+    g = np.asarray(gpu_lse, np.float64)
+    assert np.array_equal(fin, np.isfinite(g))
+    if not fin.any():
+        return 0.0, 0.0
+    bound = lse_bound(q_row, kv_hat, idx, sm_scale)
+    d64 = np.abs(g[fin] - lse_ref[fin])
+    assert np.all(d64 <= bound[fin]), f"lse vs float64 {d64.max():.3e}"
+    sel = np.unique(idx[idx >= 0])
+    kvb = kv_hat.copy()
+    kvb[sel] = bf16_round(kv_hat[sel])
+    _, l16 = oracle.sparse_attention_row(q_row, kvb, idx, sm_scale)
+    d16 = np.abs(g[fin] - l16[fin])
+    assert d16.max() <= LSE_BF16_ATOL, f"lse vs the bf16 path {d16.max():.3e}"
+    return d64.max(), d16.max()
 
 
 def check_sfa(gpu_o, ref_o):

@@ -28,15 +28,16 @@ def _end_to_end(dsa, wl, rows):
     out = out.float().cpu().numpy()
     orc = OracleRows(wl)
     qs = wl.q_sfa(rows).double().numpy()
-    compared = 0
+    same = 0
     for i, r in enumerate(rows):
         ref_idx, s, mag = orc.topk(r)
         ndiff = check_topk(idx[r], vals[r].cpu().numpy(), s, mag, wl.topk)
-        if not ndiff:   # same selection: the attention outputs must agree
-            o_ref, _ = orc.sfa(r, ref_idx, qs[i])
-            check_sfa(out[r], o_ref)
-            compared += 1
-    assert compared >= 1
+        same += ndiff == 0
+        # the attention over the GPU's own selection (equal to the oracle's up to
+        # exchanges inside the tie band, which check_topk has just bounded)
+        o_ref, _ = orc.sfa(r, idx[r], qs[i])
+        check_sfa(out[r], o_ref)
+    print(f"{wl.name}: {len(rows)} rows compared, {same} with the oracle's exact selection")
 
 
 @pytest.mark.parametrize("name", ["tiny", "short_ctx"])

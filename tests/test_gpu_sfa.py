@@ -1,6 +1,8 @@
 """GPU parity of Sparse Flash Attention against the float64 oracle (max-abs 2e-2,
-mean-abs 2e-3 on the bf16 output; lse within 1e-3), fed with the oracle's own Top-K
-indices, plus padding, empty rows, out-of-range indices and fewer heads."""
+mean-abs 2e-3 on the bf16 output; lse within the bf16 rounding's worst case of the float64
+oracle and within 1e-4 of the oracle over the bf16-rounded latent rows), fed with the
+oracle's own Top-K indices, plus padding, empty rows, out-of-range indices and fewer
+heads."""
 
 import math
 
@@ -10,7 +12,7 @@ import torch
 
 import oracle
 from dsa_sparse_attention_topk_gb300 import workloads as W
-from dsa_testlib import ensure_built, DeviceWorkload, OracleRows, check_sfa, lse_bound
+from dsa_testlib import ensure_built, DeviceWorkload, OracleRows, check_sfa, check_lse
 
 pytestmark = pytest.mark.gpu
 
@@ -51,10 +53,7 @@ def test_sfa_matches_oracle(dsa, name):
         o_ref, lse_ref = orc.sfa(r, idx[r], qs[r])
         check_sfa(out[r], o_ref)
         kvh = orc.kv_hat_rows(int(wl.q_seq[r]), idx[r])
-        fin = np.isfinite(lse_ref)
-        assert np.array_equal(fin, np.isfinite(lse[r]))
-        bound = lse_bound(qs[r], kvh, idx[r], wl.sm_scale)
-        assert np.all(np.abs(lse[r][fin] - lse_ref[fin]) <= bound[fin])
+        check_lse(lse[r], qs[r], kvh, idx[r], wl.sm_scale, lse_ref)
 
 
 def test_sfa_padding_order_empty_and_bad_index(dsa):
@@ -86,7 +85,7 @@ def test_sfa_padding_order_empty_and_bad_index(dsa):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["decode_b32_ctx32k", "long_mtp_b4_ctx128k", "prefill_4k_over_64k"])
+@pytest.mark.parametrize("name", ["decode_b32_ctx32k", "mixed_b128", "long_mtp_b4_ctx128k", "prefill_4k_over_64k"])
 def test_sfa_full_size_sampled(dsa, name):
     wl = W.make(name)
     dw = DeviceWorkload(wl)
@@ -104,8 +103,7 @@ def test_sfa_full_size_sampled(dsa, name):
         o_ref, lse_ref = orc.sfa(r, idx[r], qs[i])
         check_sfa(out[r], o_ref)
         kvh = orc.kv_hat_rows(int(wl.q_seq[r]), idx[r])
-        bound = lse_bound(qs[i], kvh, idx[r], wl.sm_scale)
-        assert np.all(np.abs(lse.cpu().numpy()[r] - lse_ref) <= bound)
+        check_lse(lse.cpu().numpy()[r], qs[i], kvh, idx[r], wl.sm_scale, lse_ref)
 
 
 def test_every_e4m3_code_dequantises_exactly(dsa):
