@@ -303,7 +303,7 @@ def run_ours(args, rank, world, local_rank):
     # dominant kernel by time share
     if t_idx >= t_sfa:
         dom, t_dom = "indexer", t_idx
-        sha = source_sha("indexer_tc.cu", "topk_cluster.cuh", "tc_utils.cuh", "dsa_common.cuh")
+        sha = source_sha("indexer_tc.cu", "topk_cluster.cuh", "tc_utils.cuh", "dsa_common.cuh", "quant_tok.cuh")
         ach = idx_bytes / (t_dom * 1e-3) / 1e9
         roof = {"kernel": "indexer_topk", "bound": "hbm", "achieved": round(ach, 1), "peak": hbm,
                 "unit": "GB/s", "frac": round(ach / hbm, 4), "peak_source": peaks_src,
