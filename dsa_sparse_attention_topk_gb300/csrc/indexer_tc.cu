@@ -29,6 +29,7 @@
 // (topk_cluster.cuh).
 
 #include <algorithm>
+#include <mutex>
 #include <cfloat>
 #include <cuda.h>
 
@@ -62,6 +63,7 @@ constexpr int kStageBytes = kStageA + 2 * kStageSF;  // + transposed copy: 17408
 constexpr int kProd = 2;              // producer lanes (the ring size is a multiple of it)
 constexpr int kMaxCluster = 16;
 constexpr int kMaxStages = 8;
+constexpr int kLptMaxGroups = 256;    // launches with more row groups keep the grid order
 
 struct Plan {
   int G, H, Hp, Np, nacc, stages, chunk_cap;
@@ -124,6 +126,22 @@ __host__ inline Plan make_plan(int G, int H, int chunk_cap, int stages) {
   return p;
 }
 
+// Number of positions row group [row0, row0 + G) scans: the largest selectable count of its
+// rows (0 for an invalid sequence; the kernel prologue reports bad inputs).
+__device__ inline uint32_t group_scan_len(const IndexerArgs& a, int row0, int G) {
+  const int seq = __ldcg(a.q_seq + row0);
+  if (seq < 0 || seq >= a.n_seq) return 0u;
+  int L = __ldcg(a.seq_lens + seq);
+  L = L < 0 ? 0 : (L > a.max_ctx ? a.max_ctx : L);
+  uint32_t n = 0;
+  for (int j = 0; j < G; ++j) {
+    long long v = static_cast<long long>(__ldcg(a.q_pos + row0 + j)) + 1;
+    v = v < 0 ? 0 : (v > L ? L : v);
+    n = max(n, static_cast<uint32_t>(v));
+  }
+  return n;
+}
+
 // MXFP8-quantise one 128-wide bf16 row (this lane's four values, already loaded) straight
 // into the B operand (128-byte swizzled K-major row n) and return this lane's group
 // exponent code (lanes 0, 8, 16, 24 hold groups 0..3).  Same OCP MX rule as the cache writer.
@@ -162,7 +180,6 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = static_cast<int>(cluster_ctarank());
   const int C = static_cast<int>(cluster_nctarank());
-  const int row0 = blockIdx.y * G;
   const int H = pl.H, S = pl.stages;
   constexpr int Hp = HP, Np = G * HP;
   constexpr int kThreads = threads_for(Np), kMma = mma_warps(Np), kNacc = acc_count(Np);
@@ -175,6 +192,29 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
   // kernel is the cache writer of a decode step (early_inputs): then only the K-cache, the
   // writer's output, waits (the producer lanes, below); the reads before it bypass L1
   if (!a.early_inputs) pdl_wait();
+  // Which row group this cluster takes: the groups in order of decreasing scan length (ties
+  // in group order), so that when the grid runs in several waves the clusters of the
+  // longest groups are dispatched first and the short ones fill in behind them.  Every CTA
+  // of the cluster computes the same ranking.
+  int group = static_cast<int>(blockIdx.y);
+  const int n_groups = static_cast<int>(gridDim.y);
+  if (n_groups > 1 && n_groups <= kLptMaxGroups) {
+    uint32_t* s_len = reinterpret_cast<uint32_t*>(smem + pl.off_stage);  // the copy ring is idle yet
+    for (int g = tid; g < n_groups; g += kThreads) s_len[g] = group_scan_len(a, g * G, G);
+    __syncthreads();
+    for (int g = tid; g < n_groups; g += kThreads) {
+      const uint32_t v = s_len[g];
+      int r = 0;
+      for (int h = 0; h < n_groups; ++h) {
+        const uint32_t u = s_len[h];
+        r += (u > v || (u == v && h < g)) ? 1 : 0;
+      }
+      if (r == static_cast<int>(blockIdx.y)) s_len[kLptMaxGroups] = static_cast<uint32_t>(g);
+    }
+    __syncthreads();
+    group = static_cast<int>(s_len[kLptMaxGroups]);
+  }
+  const int row0 = group * G;
   if (tid == 0) {
     int seq = __ldcg(a.q_seq + row0);
     unsigned bad = 0;
@@ -517,21 +557,111 @@ EncodeFn encode_fn() {
   return fn;
 }
 
+// Clusters of c CTAs that fit on the GPU at once with one CTA per SM (the indexer's shared
+// memory): the GPCs' SM counts are not multiples of most cluster sizes, so this is below
+// n_sm / c (on a 152-SM part: 36 clusters of 4, 15 of 8, 8 of 12, 7 of 16).  Queried once
+// per device and size, under a lock.
+__global__ void cluster_fit_probe_kernel(int) {}
+int clusters_that_fit(int c, int n_sm) {
+  if (c <= 1) return n_sm;
+  static std::mutex mu;
+  static int cache[64][kMaxCluster + 1] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || c > kMaxCluster) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev][c]) return cache[dev][c];
+  const int smem = 120 * 1024;
+  if (cudaFuncSetAttribute(cluster_fit_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+      cudaFuncSetAttribute(cluster_fit_probe_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(c), 1, 1);
+  cfg.blockDim = dim3(32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, cluster_fit_probe_kernel, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  cache[dev][c] = n;
+  return n;
+}
+
+// Positions per CTA for a cluster of c CTAs over max_ctx positions.
+inline int cap_for(int max_ctx, int c) {
+  const int chunk = (max_ctx + c - 1) / c;
+  return (chunk + kTileP - 1) / kTileP * kTileP;
+}
+
+// Grid shape: rows per group and CTAs per cluster.
+struct GridChoice {
+  int G = 0, C = 0;
+};
+
+// The cluster size (1..16, any size) that gives the most CTAs while every group's cluster
+// is resident at once, for groups of g rows; 0 if no size does (more groups than one wave).
+int single_wave_cluster(int g, int n_q, int h_i, int max_ctx, int n_sm, size_t limit, long long* ctas) {
+  const int n_groups = n_q / g;
+  int best = 0;
+  *ctas = 0;
+  for (int c = 1; c <= kMaxCluster; ++c) {
+    if (make_plan(g, h_i, cap_for(max_ctx, c), 4).total > limit) continue;
+    if (clusters_that_fit(c, n_sm) < n_groups) continue;
+    const long long n = static_cast<long long>(n_groups) * c;
+    if (n > *ctas) {
+      *ctas = n;
+      best = c;
+    }
+  }
+  return best;
+}
+
+GridChoice choose_grid(int q_group, int n_q, int h_i, int max_ctx, int n_sm, size_t limit) {
+  GridChoice r;
+  long long ctas = 0;
+  const int C = single_wave_cluster(q_group, n_q, h_i, max_ctx, n_sm, limit, &ctas);
+  // Few long row groups would leave most of the GPU idle even with the largest clusters:
+  // scan the rows of a group one by one (each row its own cluster) when that puts more
+  // CTAs to work; the shared reads of the group are then repeated, the selection is not.
+  if (q_group > 1 && 2 * ctas < n_sm) {
+    long long ctas1 = 0;
+    const int C1 = single_wave_cluster(1, n_q, h_i, max_ctx, n_sm, limit, &ctas1);
+    if (C1 && ctas1 > ctas) {
+      r.G = 1;
+      r.C = C1;
+      return r;
+    }
+  }
+  r.G = q_group;
+  if (C) {
+    r.C = C;
+    return r;
+  }
+  // more groups than one wave holds: the smallest power of two whose score buffer fits next
+  // to a 4-stage ring, widened while the grid still fits on the GPU in one wave
+  int c = 1;
+  while (c < kMaxCluster && make_plan(q_group, h_i, cap_for(max_ctx, c), 4).total > limit) c *= 2;
+  while (c < kMaxCluster && static_cast<long long>(n_q / q_group) * c * 2 <= n_sm) c *= 2;
+  r.C = c;
+  return r;
+}
+
 template <int G, int HP>
-cudaError_t launch_gh(const IndexerArgs& a, cudaStream_t s, const char** err) {
+cudaError_t launch_gh(const IndexerArgs& a, cudaStream_t s, const char** err, int C) {
   DevInfo di;
   if (!device_info(&di, err)) return cudaErrorInvalidDevice;
   const int n_groups = a.n_q / G;
   const size_t limit = static_cast<size_t>(di.smem_optin) - 1024;  // room for the 1024-byte alignment
-  auto cap_for = [&](int c) {
-    int chunk = (a.max_ctx + c - 1) / c;
-    return (chunk + kTileP - 1) / kTileP * kTileP;
-  };
-  // smallest power-of-two cluster whose score buffer fits next to a 4-stage ring, then
-  // widen while the grid still fits on the GPU in one wave
-  int C = 1;
-  while (C < kMaxCluster && make_plan(G, a.h_i, cap_for(C), 4).total > limit) C *= 2;
-  while (C < kMaxCluster && static_cast<long long>(n_groups) * C * 2 <= di.n_sm) C *= 2;
+  auto cap_for = [&](int c) { return dsa::cap_for(a.max_ctx, c); };
   int stages = kMaxStages;
   // a multiple of kProd (and so of the two MMA issuers): every stage keeps one issuer and
   // one waiter per barrier
@@ -577,11 +707,11 @@ cudaError_t launch_gh(const IndexerArgs& a, cudaStream_t s, const char** err) {
 }
 
 template <int G>
-cudaError_t launch_g(const IndexerArgs& a, cudaStream_t s, const char** err) {
+cudaError_t launch_g(const IndexerArgs& a, cudaStream_t s, const char** err, int C) {
   switch (padded_heads(a.h_i)) {
-    case 16: return launch_gh<G, 16>(a, s, err);
-    case 32: return launch_gh<G, 32>(a, s, err);
-    default: return launch_gh<G, 64>(a, s, err);
+    case 16: return launch_gh<G, 16>(a, s, err, C);
+    case 32: return launch_gh<G, 32>(a, s, err, C);
+    default: return launch_gh<G, 64>(a, s, err, C);
   }
 }
 
@@ -589,12 +719,19 @@ cudaError_t launch_g(const IndexerArgs& a, cudaStream_t s, const char** err) {
 
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s, const char** err) {
   if (a.n_q == 0) return cudaSuccess;
-  switch (a.q_group) {
-    case 1: return launch_g<1>(a, s, err);
-    case 2: return launch_g<2>(a, s, err);
-    case 3: return launch_g<3>(a, s, err);
-    case 4: return launch_g<4>(a, s, err);
-    default: *err = "indexer: q_group must be 1..4"; return cudaErrorInvalidValue;
+  if (a.q_group < 1 || a.q_group > 4) {
+    *err = "indexer: q_group must be 1..4";
+    return cudaErrorInvalidValue;
+  }
+  DevInfo di;
+  if (!device_info(&di, err)) return cudaErrorInvalidDevice;
+  const GridChoice g = choose_grid(a.q_group, a.n_q, a.h_i, a.max_ctx, di.n_sm,
+                                   static_cast<size_t>(di.smem_optin) - 1024);
+  switch (g.G) {
+    case 1: return launch_g<1>(a, s, err, g.C);
+    case 2: return launch_g<2>(a, s, err, g.C);
+    case 3: return launch_g<3>(a, s, err, g.C);
+    default: return launch_g<4>(a, s, err, g.C);
   }
 }
 
