@@ -602,6 +602,9 @@ inline int cap_for(int max_ctx, int c) {
   return (chunk + kTileP - 1) / kTileP * kTileP;
 }
 
+// The cost of one row's selection, in positions scanned (about 10 us, the cluster Top-K).
+constexpr int kSelectAllowance = 2048;
+
 // Grid shape: rows per group and CTAs per cluster.
 struct GridChoice {
   int G = 0, C = 0;
@@ -646,12 +649,33 @@ GridChoice choose_grid(int q_group, int n_q, int h_i, int max_ctx, int n_sm, siz
     r.C = C;
     return r;
   }
-  // more groups than one wave holds: the smallest power of two whose score buffer fits next
-  // to a 4-stage ring, widened while the grid still fits on the GPU in one wave
-  int c = 1;
-  while (c < kMaxCluster && make_plan(q_group, h_i, cap_for(max_ctx, c), 4).total > limit) c *= 2;
-  while (c < kMaxCluster && static_cast<long long>(n_q / q_group) * c * 2 <= n_sm) c *= 2;
-  r.C = c;
+  // More groups than one wave holds: the grouping (the caller's, or one row per group) and
+  // cluster size of least estimated time, waves x rows per group x (positions per CTA + an
+  // allowance for each row's selection).  The scan's cost follows rows x positions (the
+  // MMA's N and the epilogue grow with the rows of a group), so resident CTAs count more
+  // than shared reads: prefill rows over a 64K prefix run 2.2x faster as single rows in
+  // clusters of 4 (36 resident) than as groups of 4 in clusters of 16 (7 resident).
+  double best = 0.0;
+  for (int k = 0; k < (q_group > 1 ? 2 : 1); ++k) {
+    const int g = k == 0 ? q_group : 1;
+    const long long n_groups = n_q / g;
+    for (int c = 1; c <= kMaxCluster; ++c) {
+      if (make_plan(g, h_i, cap_for(max_ctx, c), 4).total > limit) continue;
+      const int fit = clusters_that_fit(c, n_sm);
+      if (fit < 1) continue;
+      const long long waves = (n_groups + fit - 1) / fit;
+      const double cost = static_cast<double>(waves) * g * (cap_for(max_ctx, c) + kSelectAllowance);
+      if (!r.C || cost < best) {
+        best = cost;
+        r.G = g;
+        r.C = c;
+      }
+    }
+  }
+  if (!r.C) {  // nothing fits (the launch reports it): the caller's grouping
+    r.G = q_group;
+    r.C = kMaxCluster;
+  }
   return r;
 }
 
