@@ -116,7 +116,7 @@ __host__ inline Plan make_plan(int G, int H, int chunk_cap, int stages) {
   p.off_stage = o; o += stages * kStageBytes;
   p.off_b = o = align_up(o, 1024); o += p.Np * kIdxDim;
   p.off_sfb = o = align_up(o, 16); o += 2 * 512;
-  p.off_w = o; o += 4 * G * p.Hp;
+  p.off_w = o = align_up(o, 16); o += 4 * G * p.Hp;  // read as float4
   p.off_keys = o = align_up(o, 16); o += 4u * G * chunk_cap;
   p.off_hist0 = o; o += 4u * G * kHistBins;
   p.off_pages = o; o += 4u * (chunk_cap / kPage + 2);
@@ -489,10 +489,18 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
 #pragma unroll
         for (int h0 = 0; h0 < HP; h0 += 16) tc::tmem_ld16(col + h0, reinterpret_cast<uint32_t(&)[16]>(r[h0]));
         tc::tmem_wait_ld();
-        const float* wj = s_w + j * HP;
+        // the weights are read four at a time (one 16-byte shared load for four heads):
+        // with a load per head the shared-memory pipe, not the arithmetic, set the pace
+        const float4* w4 = reinterpret_cast<const float4*>(s_w + j * HP);
         float s4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains over the heads
 #pragma unroll
-        for (int h = 0; h < HP; ++h) s4[h & 3] = fmaf(wj[h], relu_nan(__uint_as_float(r[h])), s4[h & 3]);
+        for (int h = 0; h < HP; h += 4) {
+          const float4 w = w4[h >> 2];
+          s4[0] = fmaf(w.x, relu_nan(__uint_as_float(r[h])), s4[0]);
+          s4[1] = fmaf(w.y, relu_nan(__uint_as_float(r[h + 1])), s4[1]);
+          s4[2] = fmaf(w.z, relu_nan(__uint_as_float(r[h + 2])), s4[2]);
+          s4[3] = fmaf(w.w, relu_nan(__uint_as_float(r[h + 3])), s4[3]);
+        }
         sc[j] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
       }
       tc::fence_before_sync();
