@@ -64,12 +64,16 @@ constexpr int kProd = 2;              // producer lanes (the ring size is a mult
 constexpr int kMaxCluster = 16;
 constexpr int kMaxStages = 8;
 constexpr int kLptMaxGroups = 256;    // launches with more row groups keep the grid order
+// The selector's scratch and its candidate list live in the copy ring once the scan is done,
+// which leaves room for a deeper ring: the scratch at the start, the candidates after it.
+constexpr int kTopkBytes = (static_cast<int>(sizeof(TopkSmem)) + 15) / 16 * 16;
+static_assert(kTopkBytes < kProd * kStageBytes, "the smallest ring holds the selector's scratch");
 
 struct Plan {
   int G, H, Hp, Np, nacc, stages, chunk_cap;
   uint32_t tmem_cols, d_col[kMaxAcc], sfa_col[kMaxAcc], sfb_col;
   // dynamic shared memory offsets (from a 1024-byte aligned base)
-  uint32_t off_stage, off_b, off_sfb, off_w, off_keys, off_hist0, off_pages, off_topk, off_bar, total;
+  uint32_t off_stage, off_b, off_sfb, off_w, off_keys, off_hist0, off_pages, off_bar, total;
 };
 
 // Query heads padded to the MMA's N granularity: 16, 32 or 64 rows per query row.
@@ -120,7 +124,6 @@ __host__ inline Plan make_plan(int G, int H, int chunk_cap, int stages) {
   p.off_keys = o = align_up(o, 16); o += 4u * G * chunk_cap;
   p.off_hist0 = o; o += 4u * G * kHistBins;
   p.off_pages = o; o += 4u * (chunk_cap / kPage + 2);
-  p.off_topk = o = align_up(o, 16); o += sizeof(TopkSmem);
   p.off_bar = o = align_up(o, 16); o += sizeof(Barriers);
   p.total = o;
   return p;
@@ -170,7 +173,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   Barriers& bs = *reinterpret_cast<Barriers*>(smem + pl.off_bar);
-  TopkSmem& tk = *reinterpret_cast<TopkSmem*>(smem + pl.off_topk);
+  TopkSmem& tk = *reinterpret_cast<TopkSmem*>(smem + pl.off_stage);  // used after the scan only
   uint8_t* s_b = smem + pl.off_b;
   uint32_t* s_sfb = reinterpret_cast<uint32_t*>(smem + pl.off_sfb);
   float* s_w = reinterpret_cast<float*>(smem + pl.off_w);
@@ -185,7 +188,6 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
   constexpr int kThreads = threads_for(Np), kMma = mma_warps(Np), kNacc = acc_count(Np);
 
   // ---- prologue -------------------------------------------------------------------
-  topk_init(tk);
   for (int i = tid; i < G * kHistBins; i += kThreads) s_hist0[i] = 0;
   pdl_launch_dependents();
   // nothing global is read before the previous kernel on the stream is done, unless that
@@ -519,13 +521,14 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
     }
   }
   tc::fence_before_sync();
-  __syncthreads();
+  __syncthreads();  // the ring is idle: every copy into it has landed, every MMA has read it
+  topk_init(tk);
   cluster_sync();  // every CTA of the cluster has initialised its selector before DSMEM traffic
 
   if (a.out_idx) {
-    // the copy ring is idle now: it holds the selector's candidate lists
-    uint2* cand = reinterpret_cast<uint2*>(smem + pl.off_stage);
-    const int cand_cap = pl.stages * kStageBytes / static_cast<int>(sizeof(uint2));
+    // the copy ring is idle now: after the selector's scratch it holds the candidate lists
+    uint2* cand = reinterpret_cast<uint2*>(smem + pl.off_stage + kTopkBytes);
+    const int cand_cap = (pl.stages * kStageBytes - kTopkBytes) / static_cast<int>(sizeof(uint2));
 #pragma unroll 1
     for (int j = 0; j < G; ++j) {
       const size_t row = static_cast<size_t>(row0 + j);
