@@ -71,6 +71,7 @@ static_assert(kTopkBytes < kProd * kStageBytes, "the smallest ring holds the sel
 
 struct Plan {
   int G, H, Hp, Np, nacc, stages, chunk_cap;
+  int ranked;  // the launch runs in several waves: clusters take the row groups longest first
   uint32_t tmem_cols, d_col[kMaxAcc], sfa_col[kMaxAcc], sfb_col;
   // dynamic shared memory offsets (from a 1024-byte aligned base)
   uint32_t off_stage, off_b, off_sfb, off_w, off_keys, off_hist0, off_pages, off_bar, total;
@@ -200,7 +201,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
   // of the cluster computes the same ranking.
   int group = static_cast<int>(blockIdx.y);
   const int n_groups = static_cast<int>(gridDim.y);
-  if (n_groups > 1 && n_groups <= kLptMaxGroups) {
+  if (pl.ranked && n_groups <= kLptMaxGroups) {
     uint32_t* s_len = reinterpret_cast<uint32_t*>(smem + pl.off_stage);  // the copy ring is idle yet
     for (int g = tid; g < n_groups; g += kThreads) s_len[g] = group_scan_len(a, g * G, G);
     __syncthreads();
@@ -701,7 +702,8 @@ cudaError_t launch_gh(const IndexerArgs& a, cudaStream_t s, const char** err, in
   // a multiple of kProd (and so of the two MMA issuers): every stage keeps one issuer and
   // one waiter per barrier
   while (stages > kProd && make_plan(G, a.h_i, cap_for(C), stages).total > limit) stages -= kProd;
-  const Plan pl = make_plan(G, a.h_i, cap_for(C), stages);
+  Plan pl = make_plan(G, a.h_i, cap_for(C), stages);
+  pl.ranked = n_groups > clusters_that_fit(C, di.n_sm) ? 1 : 0;
   if (pl.total > limit) {
     *err = "indexer: max_ctx too large for the on-chip score buffer";
     return cudaErrorInvalidValue;
