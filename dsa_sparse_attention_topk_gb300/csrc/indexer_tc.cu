@@ -72,6 +72,7 @@ static_assert(kTopkBytes < kProd * kStageBytes, "the smallest ring holds the sel
 struct Plan {
   int G, H, Hp, Np, nacc, stages, chunk_cap;
   int ranked;  // the launch runs in several waves: clusters take the row groups longest first
+  int read_once;  // no more row groups than sequences: each K page is read by one cluster
   uint32_t tmem_cols, d_col[kMaxAcc], sfa_col[kMaxAcc], sfb_col;
   // dynamic shared memory offsets (from a 1024-byte aligned base)
   uint32_t off_stage, off_b, off_sfb, off_w, off_keys, off_hist0, off_pages, off_bar, total;
@@ -321,6 +322,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
       // enough to keep the HBM busy, and with a ring of a multiple of kProd stages each
       // stage keeps one issuer
       if (lane == 0) tc::prefetch_tmap(&kmap);
+      // pages that no other cluster reads are streamed evict-first: a stream larger than L2
+      // would otherwise evict the kernel's own instructions and the other inputs
+      const uint64_t pol = pl.read_once ? tc::l2_policy_evict_first() : tc::l2_policy_evict_normal();
       int last = -1;  // the last tile this lane issued
       for (int t = a.stall_producer ? ntiles : lane; t < ntiles; t += kProd) {
         const int s = t % S, it = t / S;
@@ -333,14 +337,14 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
         const uint32_t bytes = (pg0 >= 0 ? (kKPageBytes) : 0) + (pg1 >= 0 ? (kKPageBytes) : 0);
         tc::mbar_arrive_expect_tx(&bs.full[s], bytes);
         if (pg0 >= 0) {
-          tc::tma_load_3d(st, &kmap, 0, 0, pg0, &bs.full[s]);
-          tc::bulk_load(st + kStageA, a.k_cache + static_cast<int64_t>(pg0) * kKPageBytes + kKScaleOff, 256,
-                        &bs.full[s]);
+          tc::tma_load_3d_hint(st, &kmap, 0, 0, pg0, &bs.full[s], pol);
+          tc::bulk_load_hint(st + kStageA, a.k_cache + static_cast<int64_t>(pg0) * kKPageBytes + kKScaleOff, 256,
+                             &bs.full[s], pol);
         }
         if (pg1 >= 0) {
-          tc::tma_load_3d(st + kStageA / 2, &kmap, 0, 0, pg1, &bs.full[s]);
-          tc::bulk_load(st + kStageA + 256, a.k_cache + static_cast<int64_t>(pg1) * kKPageBytes + kKScaleOff, 256,
-                        &bs.full[s]);
+          tc::tma_load_3d_hint(st + kStageA / 2, &kmap, 0, 0, pg1, &bs.full[s], pol);
+          tc::bulk_load_hint(st + kStageA + 256, a.k_cache + static_cast<int64_t>(pg1) * kKPageBytes + kKScaleOff, 256,
+                             &bs.full[s], pol);
         }
         last = t;
       }
@@ -704,6 +708,7 @@ cudaError_t launch_gh(const IndexerArgs& a, cudaStream_t s, const char** err, in
   while (stages > kProd && make_plan(G, a.h_i, cap_for(C), stages).total > limit) stages -= kProd;
   Plan pl = make_plan(G, a.h_i, cap_for(C), stages);
   pl.ranked = n_groups > clusters_that_fit(C, di.n_sm) ? 1 : 0;
+  pl.read_once = n_groups <= a.n_seq ? 1 : 0;
   if (pl.total > limit) {
     *err = "indexer: max_ctx too large for the on-chip score buffer";
     return cudaErrorInvalidValue;
