@@ -131,6 +131,12 @@ __device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void dsmem_st_v2(uint32_t addr, uint2 v) {
   asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" :: "r"(addr), "r"(v.x), "r"(v.y) : "memory");
 }
+// Store 8 bytes into another CTA's shared memory and count them on that CTA's mbarrier
+// (complete-tx): the receiver learns that the data has landed from the barrier alone.
+__device__ __forceinline__ void dsmem_st_async_v2(uint32_t addr, uint2 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.u32 [%0], {%1, %2}, [%3];"
+               :: "r"(addr), "r"(v.x), "r"(v.y), "r"(bar) : "memory");
+}
 __device__ __forceinline__ uint4 dsmem_ld_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"

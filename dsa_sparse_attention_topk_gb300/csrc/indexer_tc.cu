@@ -538,7 +538,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
     for (int j = 0; j < G; ++j) {
       const size_t row = static_cast<size_t>(row0 + j);
       cluster_topk_row(tk, s_keys + j * pl.chunk_cap, s_hist0 + j * kHistBins, c0, chunk, len, bs.n_sel[j], a.topk,
-                       a.out_idx + row * a.topk, a.out_scores ? a.out_scores + row * a.topk : nullptr, cand, cand_cap);
+                       a.out_idx + row * a.topk, a.out_scores ? a.out_scores + row * a.topk : nullptr, cand, cand_cap,
+                       j, a.status, wait_ns);
     }
   }
   // every CTA has waited for the writer before it leaves, so this grid never completes

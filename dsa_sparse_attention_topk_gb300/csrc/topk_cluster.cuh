@@ -14,7 +14,9 @@
 // keys above bin d0 and in it, and the counts are exchanged (second barrier).  Each CTA
 // writes its keys above d0 straight to the output at its rank's offset, and its keys in
 // bin d0 with their positions into the leader's list at its rank's offset, both in
-// position order (third barrier).  The leader finishes alone over those few candidates:
+// position order.  The list entries are asynchronous stores that the leader's mbarrier
+// counts (it expects the bin's cluster-wide count), so neither the list nor the output
+// writes wait on a cluster barrier.  The leader finishes alone over those few candidates:
 // the last two digits, then the keys > T and the lowest positions with key == T.
 //
 // Otherwise (a top bin too crowded for the list) the last two digits go through the
@@ -25,7 +27,10 @@
 // Either way the output is deterministic.
 #pragma once
 
+#include <cstddef>
+
 #include "dsa_common.cuh"
+#include "tc_utils.cuh"
 
 namespace dsa {
 
@@ -36,16 +41,25 @@ struct TopkSmem {
   uint32_t hist[2][kHistBins];   // [0]: the cluster's first-digit histogram (every CTA);
                                  // leader: cluster histograms of the later digits
   uint32_t local[kHistBins];     // this CTA's histogram of the current digit
-  uint32_t counts[2][16];        // per-rank counts
+  uint32_t counts[2][2][16];     // per-rank counts, one table per row parity
   uint32_t bcast[2];             // (digit, count_above) sent by the leader
   uint32_t pick[4];              // results of this CTA's own picks
   uint32_t warp_cnt[2][32];      // per-warp counts for the ordered compactions
-  uint32_t seg_off[16 * 32 + 1]; // leader: offsets of the (rank, warp) list segments
+  uint32_t cand_uses;            // leader: rows whose candidates came through cand_bar
+  uint64_t cand_bar;             // leader: completes once a row's candidates have landed
 };
+static_assert(offsetof(TopkSmem, hist) % 16 == 0 && offsetof(TopkSmem, local) % 16 == 0,
+              "the histograms are accessed 16 bytes at a time");
 
-// Zero the histograms; call before the first cluster_sync of the kernel.
+// Zero the histograms and set up the candidate barrier; call with every thread before the
+// cluster barrier that precedes any DSMEM traffic.
 __device__ __forceinline__ void topk_init(TopkSmem& sm) {
   for (int i = threadIdx.x; i < 2 * kHistBins; i += blockDim.x) (&sm.hist[0][0])[i] = 0;
+  if (threadIdx.x == 0) {
+    sm.cand_uses = 0;
+    tc::mbar_init(&sm.cand_bar, 1);
+    tc::mbar_fence_init();
+  }
 }
 
 // Add `key`'s top digit (bits 31..21) to a local histogram, aggregated over the warp.
@@ -225,7 +239,7 @@ __device__ void leader_finish(TopkSmem& sm, const uint2* cand, uint32_t n, uint3
 // of the first need_eq keys == T (rank order is position order) to the output; returns the
 // cluster-wide count of keys > T.  Called by every thread of every CTA of the cluster.
 __device__ uint32_t cluster_write_selected(TopkSmem& sm, const uint32_t* keys, int c0, int len, uint32_t T,
-                                          uint32_t need_eq, int K, int32_t* out_idx, float* out_scores) {
+                                          uint32_t need_eq, int K, int32_t* out_idx, float* out_scores, int par) {
   const uint32_t rank = cluster_ctarank();
   const uint32_t nrank = cluster_nctarank();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
@@ -244,13 +258,13 @@ __device__ uint32_t cluster_write_selected(TopkSmem& sm, const uint32_t* keys, i
   if (tid < static_cast<int>(nrank)) {  // push this rank's counts into every rank's table
     uint32_t my_gt = 0, my_eq = 0;
     for (int w = 0; w < nw; ++w) { my_gt += sm.warp_cnt[0][w]; my_eq += sm.warp_cnt[1][w]; }
-    dsmem_st_u32(dsmem_addr(&sm.counts[0][rank], tid), my_gt);
-    dsmem_st_u32(dsmem_addr(&sm.counts[1][rank], tid), my_eq);
+    dsmem_st_u32(dsmem_addr(&sm.counts[par][0][rank], tid), my_gt);
+    dsmem_st_u32(dsmem_addr(&sm.counts[par][1][rank], tid), my_eq);
   }
   cluster_sync();
   uint32_t gt_before = 0, eq_before = 0, gt_total = 0;
   for (uint32_t r = 0; r < nrank; ++r) {
-    const uint32_t a = sm.counts[0][r], b = sm.counts[1][r];
+    const uint32_t a = sm.counts[par][0][r], b = sm.counts[par][1][r];
     if (r < rank) { gt_before += a; eq_before += b; }
     gt_total += a;
   }
@@ -298,11 +312,16 @@ __device__ uint32_t cluster_write_selected(TopkSmem& sm, const uint32_t* keys, i
 //   n_sel         number of selectable positions of the row (positions 0..n_sel-1)
 //   cand          cand_cap free (key, position) slots of shared memory, at the same offset
 //                 in every CTA of the cluster (the leader's copy receives the candidates)
+//   row           index of this call among the kernel's calls (its parity picks the count
+//                 table, so a CTA that runs ahead never overwrites counts still being read)
+//   status, wait_ns  the leader's wait for the candidates gives up after wait_ns and sets
+//                 the TIMEOUT status bit
 // Writes out_idx[0..K) (and out_scores if non-null).  Must be called by every thread of
 // every CTA of the cluster (it contains cluster barriers).  The caller must pass another
 // cluster barrier before `cand` or the selector's scratch is written again.
 __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, const uint32_t* hist0, int c0, int chunk, int len,
-                                 int n_sel, int K, int32_t* out_idx, float* out_scores, uint2* cand, int cand_cap) {
+                                 int n_sel, int K, int32_t* out_idx, float* out_scores, uint2* cand, int cand_cap,
+                                 int row, unsigned* status, uint64_t wait_ns) {
   const uint32_t rank = cluster_ctarank();
   const uint32_t nrank = cluster_nctarank();
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
@@ -345,7 +364,7 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, const uint3
   if (!found) {
     // fewer than K selectable keys although n_sel > K (positions on pages flagged bad):
     // keep every selectable key, in position order, and pad the rest of the row with -1
-    const uint32_t n_valid = cluster_write_selected(sm, keys, c0, len, 0u, 0u, K, out_idx, out_scores);
+    const uint32_t n_valid = cluster_write_selected(sm, keys, c0, len, 0u, 0u, K, out_idx, out_scores, row & 1);
     if (rank == 0) {
       for (int s = static_cast<int>(n_valid) + tid; s < K; s += nt) {
         out_idx[s] = -1;
@@ -357,6 +376,11 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, const uint3
 
   const uint32_t at_total = sm.pick[3];  // cluster-wide count of keys in bin d0
   if (at_total <= static_cast<uint32_t>(cand_cap)) {
+    const int par = row & 1;
+    // the leader's barrier expects at_total candidates of 8 bytes; they arrive only after
+    // the counts barrier below, so the expectation is in place first
+    const uint32_t cand_parity = sm.cand_uses & 1u;
+    if (rank == 0 && tid == 0) tc::mbar_arrive_expect_tx(&sm.cand_bar, at_total * static_cast<uint32_t>(sizeof(uint2)));
     // ---- (1) this CTA's keys above bin d0 and in it, counted per warp slice ----
     const int span = warp_span(len);
     const int lo = warp * span, hi = min(len, lo + span);
@@ -373,15 +397,18 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, const uint3
     if (tid < static_cast<int>(nrank)) {  // push this rank's totals into every rank's table
       uint32_t my_gt = 0, my_eq = 0;
       for (int w = 0; w < nw; ++w) { my_gt += sm.warp_cnt[0][w]; my_eq += sm.warp_cnt[1][w]; }
-      dsmem_st_u32(dsmem_addr(&sm.counts[0][rank], tid), my_gt);
-      dsmem_st_u32(dsmem_addr(&sm.counts[1][rank], tid), my_eq);
+      dsmem_st_u32(dsmem_addr(&sm.counts[par][0][rank], tid), my_gt);
+      dsmem_st_u32(dsmem_addr(&sm.counts[par][1][rank], tid), my_eq);
     }
     cluster_sync();  // every rank's totals are known everywhere
     uint32_t og = 0, oe = 0;  // this warp's first output slot / candidate slot
-    for (uint32_t r = 0; r < rank; ++r) { og += sm.counts[0][r]; oe += sm.counts[1][r]; }
+    for (uint32_t r = 0; r < rank; ++r) { og += sm.counts[par][0][r]; oe += sm.counts[par][1][r]; }
     for (int w = 0; w < warp; ++w) { og += sm.warp_cnt[0][w]; oe += sm.warp_cnt[1][w]; }
     // ---- (2) keys above bin d0 to the output; keys in it to the leader's candidate list,
-    // both in position order (CTA rank order is position order) ----
+    // both in position order (CTA rank order is position order).  The candidates go out as
+    // asynchronous stores counted on the leader's barrier: no cluster barrier waits for
+    // them, nor for the output writes ----
+    const uint32_t bar = dsmem_addr(&sm.cand_bar, 0);
     const uint32_t lt = (1u << lane) - 1u;
     for (int base = lo; base < hi; base += 32) {
       const int i = base + lane;
@@ -399,14 +426,28 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, const uint3
       }
       if (in) {
         const uint32_t slot = oe + __popc(be & lt);
-        if (slot < static_cast<uint32_t>(cand_cap))
-          dsmem_st_v2(dsmem_addr(&cand[slot], 0), make_uint2(k, static_cast<uint32_t>(c0 + i)));
+        if (slot < at_total)  // (a slot past the count would never be waited for)
+          dsmem_st_async_v2(dsmem_addr(&cand[slot], 0), make_uint2(k, static_cast<uint32_t>(c0 + i)), bar);
       }
       og += __popc(bg);
       oe += __popc(be);
     }
-    cluster_sync();  // the leader's candidate list is complete
-    if (rank == 0) leader_finish(sm, cand, at_total, d0, above0, K, out_idx, out_scores);
+    if (rank == 0) {
+      // every thread waits for the whole list (bounded: a count that never completes flags
+      // TIMEOUT and the row is finished with what arrived)
+      if (!tc::mbar_try_wait(&sm.cand_bar, cand_parity)) {
+        const uint64_t t0 = tc::global_ns();
+        for (uint32_t it = 0; !tc::mbar_try_wait(&sm.cand_bar, cand_parity); ++it) {
+          if ((it & 255u) == 255u && tc::global_ns() - t0 > wait_ns) {
+            flag(status, DSA_STATUS_TIMEOUT);
+            break;
+          }
+        }
+      }
+      __syncthreads();  // every thread has read the parity before it moves on
+      if (tid == 0) sm.cand_uses += 1u;
+      leader_finish(sm, cand, at_total, d0, above0, K, out_idx, out_scores);
+    }
     return;
   }
 
@@ -438,7 +479,7 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, const uint3
     need -= sm.bcast[1];
   }
   const uint32_t T = prefix;
-  cluster_write_selected(sm, keys, c0, len, T, need, K, out_idx, out_scores);  // need >= 1 ties
+  cluster_write_selected(sm, keys, c0, len, T, need, K, out_idx, out_scores, row & 1);  // need >= 1 ties
 }
 
 }  // namespace dsa
