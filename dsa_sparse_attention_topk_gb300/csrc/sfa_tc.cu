@@ -633,34 +633,72 @@ sfa_tc_kernel(const __grid_constant__ CUtensorMap qmap, SfaArgs a, SfaPlan pl) {
 
 // Merge the splits of each (row, head).  Split s holds O_s / l_s with running max m_s; with
 // M = max_s m_s and c_s = 2^(m_s - M) l_s the output is sum_s c_s (O_s / l_s) / sum_s c_s.
-__global__ void __launch_bounds__(128)
+// 64 threads per (row, head), 8 value dims each, four heads per block.  The splits are
+// taken four at a time with all their loads issued before any is used (the merge is bound
+// by the latency of those loads, not by bandwidth); a later group whose max is larger
+// rescales what has been summed so far.
+constexpr int kCombineHeads = 4;
+constexpr int kCombineBatch = 4;
+__global__ void __launch_bounds__(64 * kCombineHeads)
 sfa_combine_kernel(SfaArgs a, SfaPlan pl) {
   pdl_launch_dependents();
   pdl_wait();
-  const int t = blockIdx.x, h = blockIdx.y;
+  const int t = blockIdx.x;
+  const int h = blockIdx.y * kCombineHeads + static_cast<int>(threadIdx.x >> 6);
+  if (h >= a.h_s) return;
+  const int d = 8 * static_cast<int>(threadIdx.x & 63);
   const int ns = pl.nsplit;
-  float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, pl.ws_ml[4 * ((static_cast<size_t>(t) * ns + s) * a.h_s + h)]);
-  float csum = 0.f, wsum_x = 0.f;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int s = 0; s < ns; ++s) {
-    const size_t slot = (static_cast<size_t>(t) * ns + s) * a.h_s + h;
-    const float4 ml = *reinterpret_cast<const float4*>(pl.ws_ml + 4 * slot);
-    const float wgt = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-    const float c = wgt * ml.y;
-    csum += c;
-    wsum_x += wgt * ml.z;
-    const uint2 v = *reinterpret_cast<const uint2*>(pl.ws_o + slot * kVDim + 4 * threadIdx.x);
-    const __nv_bfloat162 v01 = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
-    const __nv_bfloat162 v23 = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
-    acc[0] += c * __low2float(v01); acc[1] += c * __high2float(v01);
-    acc[2] += c * __low2float(v23); acc[3] += c * __high2float(v23);
+  const size_t slot0 = static_cast<size_t>(t) * ns * a.h_s + h;  // split s: slot0 + s h_s
+  float M = -INFINITY, csum = 0.f, wsum_x = 0.f;
+  float acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+  for (int s0 = 0; s0 < ns; s0 += kCombineBatch) {
+    float4 ml[kCombineBatch];
+    uint4 v[kCombineBatch];
+#pragma unroll
+    for (int i = 0; i < kCombineBatch; ++i) {
+      if (s0 + i < ns) {
+        const size_t slot = slot0 + static_cast<size_t>(s0 + i) * a.h_s;
+        ml[i] = *reinterpret_cast<const float4*>(pl.ws_ml + 4 * slot);
+        v[i] = *reinterpret_cast<const uint4*>(pl.ws_o + slot * kVDim + d);
+      } else {
+        ml[i] = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    float Mn = M;
+#pragma unroll
+    for (int i = 0; i < kCombineBatch; ++i) Mn = fmaxf(Mn, ml[i].x);
+    if (Mn != M) {  // (the first group: everything so far is zero)
+      const float r = M == -INFINITY ? 0.f : exp2f(M - Mn);
+      csum *= r;
+      wsum_x *= r;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] *= r;
+      M = Mn;
+    }
+#pragma unroll
+    for (int i = 0; i < kCombineBatch; ++i) {
+      const float wgt = (ml[i].x == -INFINITY) ? 0.f : exp2f(ml[i].x - M);
+      const float c = wgt * ml[i].y;
+      csum += c;
+      wsum_x += wgt * ml[i].z;
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+        acc[2 * k] += c * __low2float(p);
+        acc[2 * k + 1] += c * __high2float(p);
+      }
+    }
   }
   const float inv = csum > 0.f ? 1.f / csum : 0.f;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(t) * a.h_s + h) * kVDim;
-  *reinterpret_cast<uint2*>(out + 4 * threadIdx.x) =
-      make_uint2(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv));
-  if (a.out_lse && threadIdx.x == 0)
+  *reinterpret_cast<uint4*>(out + d) =
+      make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
+                 pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
+  if (a.out_lse && d == 0)
     a.out_lse[static_cast<size_t>(t) * a.h_s + h] =
         wsum_x > 0.f ? (M + log2f(wsum_x)) * 0.6931471805599453f : -INFINITY;
 }
@@ -725,7 +763,8 @@ cudaError_t launch_sfa(const SfaArgs& a, cudaStream_t s, const char** err) {
   if (e != cudaSuccess) return e;
   e = launch_pdl(sfa_tc_kernel, dim3(2 * pl.nsplit, a.n_q), dim3(kThreads), kSmemBytes, s, 1, qmap, a, pl);
   if (e != cudaSuccess || pl.nsplit == 1) return e;
-  return launch_pdl(sfa_combine_kernel, dim3(a.n_q, a.h_s), dim3(128), 0, s, 1, a, pl);
+  return launch_pdl(sfa_combine_kernel, dim3(a.n_q, (a.h_s + kCombineHeads - 1) / kCombineHeads),
+                    dim3(64 * kCombineHeads), 0, s, 1, a, pl);
 }
 
 // ---- scratch for callers that cannot allocate ----------------------------------------
