@@ -219,6 +219,22 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
     group = static_cast<int>(s_len[kLptMaxGroups]);
   }
   const int row0 = group * G;
+  if (warp == 2) {
+    // while thread 0 reads the sequence information below (a chain of dependent loads),
+    // this warp pulls the next links of that chain and the sequence's page-table row towards
+    // L2 (one 128-byte line per lane), so that only the first load of each chain pays a DRAM
+    // access: the sequence lengths and the rows' positions, then the page-table row
+    for (int i = 32 * lane; i < a.n_seq && i < 32 * 32 * 4; i += 32 * 32)
+      asm volatile("prefetch.global.L2 [%0];" :: "l"(a.seq_lens + i));
+    if (lane == 0) asm volatile("prefetch.global.L2 [%0];" :: "l"(a.q_pos + row0));
+    if (lane == 1 && G > 1) asm volatile("prefetch.global.L2 [%0];" :: "l"(a.q_pos + row0 + G - 1));
+    const int sq = __ldcg(a.q_seq + row0);
+    if (sq >= 0 && sq < a.n_seq) {
+      const int32_t* prow = a.page_table + static_cast<size_t>(sq) * a.max_pages;
+      for (int i = 32 * lane; i < a.max_pages && i < 32 * 32 * 4; i += 32 * 32)
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(prow + i));
+    }
+  }
   if (tid == 0) {
     int seq = __ldcg(a.q_seq + row0);
     unsigned bad = 0;
@@ -272,16 +288,6 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
       tc::mbar_init(&bs.drain[i], 1);
     }
     tc::mbar_fence_init();
-  }
-  if (warp == 0 && lane >= 1 && lane <= 16) {
-    // warm L2 with the sequence's page-table row (one 128-byte line per lane) while lane 0
-    // reads the sequence information, so the producer's page lookups skip a DRAM access
-    const int sq = __ldcg(a.q_seq + row0);
-    if (sq >= 0 && sq < a.n_seq) {
-      const int32_t* prow = a.page_table + static_cast<size_t>(sq) * a.max_pages;
-      const int i = 32 * (lane - 1);
-      if (i < a.max_pages) asm volatile("prefetch.global.L2 [%0];" :: "l"(prow + i));
-    }
   }
   if (warp == 1) tc::tmem_alloc(&bs.tmem_base, pl.tmem_cols);
   tc::fence_before_sync();
