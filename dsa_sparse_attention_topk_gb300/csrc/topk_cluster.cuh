@@ -45,6 +45,8 @@ struct TopkSmem {
   uint32_t bcast[2];             // (digit, count_above) sent by the leader
   uint32_t pick[4];              // results of this CTA's own picks
   uint32_t warp_cnt[2][32];      // per-warp counts for the ordered compactions
+  uint32_t few[32];              // leader: the candidates that share T's top 22 bits
+  uint32_t n_few;                // leader: how many there are (only the first 32 are kept)
   uint32_t cand_uses;            // leader: rows whose candidates came through cand_bar
   uint64_t cand_bar;             // leader: completes once a row's candidates have landed
 };
@@ -173,28 +175,63 @@ __device__ __forceinline__ int warp_span(int n, int unit = 32) {
 // that bin and are already written.  Finish the last two digits over the candidates and
 // write the selected ones after them: keys > T in position order, then the lowest
 // positions with key == T.
+// The caller zeroes sm.local and sm.n_few and passes a block barrier first.
 __device__ void leader_finish(TopkSmem& sm, const uint2* cand, uint32_t n, uint32_t d0, uint32_t above0, int K,
                               int32_t* out_idx, float* out_scores) {
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
   uint32_t need = static_cast<uint32_t>(K) - above0;
-  for (int i = tid; i < kHistBins; i += nt) sm.local[i] = 0;
-  __syncthreads();
   for (uint32_t v = tid; v < n; v += nt) atomicAdd(&sm.local[(cand[v].x >> 10) & 2047u], 1u);
   __syncthreads();
   uint32_t d1, a1;
   block_pick(sm, sm.local, need, d1, a1);
   need -= a1;
   const uint32_t pre = (d0 << 11) | d1;  // bits 31..10 of T
+  // Last digit.  The candidates that share T's top 22 bits are usually a handful: they are
+  // collected, and one warp finds T as the need-th largest of them (the largest key that
+  // at least `need` of them reach).  More than 32 take a histogram of the last 10 bits.
   for (int i = tid; i < kHistBins; i += nt) sm.local[i] = 0;
-  __syncthreads();
   for (uint32_t v = tid; v < n; v += nt) {
     const uint32_t k = cand[v].x;
-    if ((k >> 10) == pre) atomicAdd(&sm.local[k & 1023u], 1u);
+    if ((k >> 10) == pre) {
+      const uint32_t slot = atomicAdd(&sm.n_few, 1u);
+      if (slot < 32u) sm.few[slot] = k;
+    }
   }
   __syncthreads();
-  uint32_t d2, a2;
-  block_pick(sm, sm.local, need, d2, a2);
-  const uint32_t T = (pre << 10) | d2;
+  uint32_t T = 0u, a2 = 0u;
+  bool found = false;
+  if (sm.n_few <= 32u) {
+    if (warp == 0) {
+      const uint32_t nf = sm.n_few;
+      const uint32_t key = static_cast<uint32_t>(lane) < nf ? sm.few[lane] : 0u;
+      uint32_t ge = 0;  // how many of them are >= this lane's key
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t kj = __shfl_sync(0xffffffffu, key, j);
+        ge += (static_cast<uint32_t>(j) < nf && kj >= key) ? 1u : 0u;
+      }
+      const bool q = static_cast<uint32_t>(lane) < nf && ge >= need;
+      const uint32_t t = __reduce_max_sync(0xffffffffu, q ? key : 0u);
+      const uint32_t above = __reduce_add_sync(0xffffffffu, (static_cast<uint32_t>(lane) < nf && key > t) ? 1u : 0u);
+      const bool ok = __any_sync(0xffffffffu, q);
+      if (lane == 0) { sm.pick[0] = t; sm.pick[1] = above; sm.pick[2] = ok ? 1u : 0u; }
+    }
+    __syncthreads();
+    found = sm.pick[2] != 0u;
+    T = sm.pick[0];
+    a2 = sm.pick[1];
+    __syncthreads();  // every thread has read the picks before they are written again
+  }
+  if (!found) {
+    for (uint32_t v = tid; v < n; v += nt) {
+      const uint32_t k = cand[v].x;
+      if ((k >> 10) == pre) atomicAdd(&sm.local[k & 1023u], 1u);
+    }
+    __syncthreads();
+    uint32_t d2;
+    block_pick(sm, sm.local, need, d2, a2);
+    T = (pre << 10) | d2;
+  }
   const uint32_t need_eq = need - a2;                     // >= 1
   const uint32_t gt_total = static_cast<uint32_t>(K) - need_eq;
 
@@ -433,6 +470,8 @@ __device__ void cluster_topk_row(TopkSmem& sm, const uint32_t* keys, const uint3
       oe += __popc(be);
     }
     if (rank == 0) {
+      for (int i = tid; i < kHistBins; i += nt) sm.local[i] = 0;  // the leader's scratch, meanwhile
+      if (tid == 0) sm.n_few = 0u;
       // every thread waits for the whole list (bounded: a count that never completes flags
       // TIMEOUT and the row is finished with what arrived)
       if (!tc::mbar_try_wait(&sm.cand_bar, cand_parity)) {
