@@ -42,16 +42,20 @@
 namespace dsa {
 namespace {
 
-constexpr int kMaxAcc = 2;
+constexpr int kMaxAcc = 4;
 
-// TMEM accumulators per CTA for N = G * HP query-head columns, and as many MMA-issuing
-// warps: accumulator i (tiles t = i mod count) belongs to issuer i and to epilogue set i.
-// A single thread can only issue a tcgen05.mma every ~120-200 cycles whatever N is, so two
-// issuers are needed to keep up with the page stream.  Each barrier that is waited on by
-// parity must see its phases in order from one waiter, which is why an accumulator never
+// TMEM accumulators per CTA for N = G * HP query-head columns, MMA-issuing warps and
+// epilogue sets.  Tile t goes to accumulator t mod acc_count, drained by epilogue set
+// t mod acc_count (four warps, one per TMEM lane quarter) and issued by warp t mod
+// mma_warps, so each set owns one accumulator and each issuer the accumulators of its
+// residue.  A single thread can only issue a tcgen05.mma every ~120-200 cycles whatever N
+// is, so two issuers are needed to keep up with the page stream.  The epilogue is a chain
+// of TMEM loads, the head sum and the key and histogram stores per position: with N <= 64
+// four sets (16 warps) hide its latencies where two cannot.  Each barrier that is waited on
+// by parity must see its phases in order from one waiter, which is why an accumulator never
 // moves between issuers and the ring has an even number of stages.
-__host__ __device__ constexpr int acc_count(int np) { return np <= 128 ? 2 : 1; }
-__host__ __device__ constexpr int mma_warps(int np) { return acc_count(np); }
+__host__ __device__ constexpr int mma_warps(int np) { return np <= 128 ? 2 : 1; }
+__host__ __device__ constexpr int acc_count(int np) { return np <= 64 ? 4 : mma_warps(np); }
 // warps: the producer, the MMA issuers, the epilogue sets, and one warp that writes a decode
 // step's new tokens (fused writes) and otherwise only helps with the query quantisation
 __host__ __device__ constexpr int threads_for(int np) { return 32 * (2 + mma_warps(np) + 4 * acc_count(np)); }
@@ -497,22 +501,29 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, IndexerArgs a, Plan 
       float sc[G];
 #pragma unroll
       for (int j = 0; j < G; ++j) {
-        uint32_t r[HP];
         const uint32_t col = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + pl.d_col[acc] + j * HP;
-#pragma unroll
-        for (int h0 = 0; h0 < HP; h0 += 16) tc::tmem_ld16(col + h0, reinterpret_cast<uint32_t(&)[16]>(r[h0]));
-        tc::tmem_wait_ld();
         // the weights are read four at a time (one 16-byte shared load for four heads):
         // with a load per head the shared-memory pipe, not the arithmetic, set the pace
         const float4* w4 = reinterpret_cast<const float4*>(s_w + j * HP);
         float s4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains over the heads
+        // with four epilogue sets the heads come in halves of 32 TMEM columns (the larger
+        // block has fewer registers per thread)
+        constexpr int kPart = (kNacc > 2 && HP > 32) ? 32 : HP;
 #pragma unroll
-        for (int h = 0; h < HP; h += 4) {
-          const float4 w = w4[h >> 2];
-          s4[0] = fmaf(w.x, relu_nan(__uint_as_float(r[h])), s4[0]);
-          s4[1] = fmaf(w.y, relu_nan(__uint_as_float(r[h + 1])), s4[1]);
-          s4[2] = fmaf(w.z, relu_nan(__uint_as_float(r[h + 2])), s4[2]);
-          s4[3] = fmaf(w.w, relu_nan(__uint_as_float(r[h + 3])), s4[3]);
+        for (int h1 = 0; h1 < HP; h1 += kPart) {
+          uint32_t r[kPart];
+#pragma unroll
+          for (int h0 = 0; h0 < kPart; h0 += 16)
+            tc::tmem_ld16(col + h1 + h0, reinterpret_cast<uint32_t(&)[16]>(r[h0]));
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < kPart; h += 4) {
+            const float4 w = w4[(h1 + h) >> 2];
+            s4[0] = fmaf(w.x, relu_nan(__uint_as_float(r[h])), s4[0]);
+            s4[1] = fmaf(w.y, relu_nan(__uint_as_float(r[h + 1])), s4[1]);
+            s4[2] = fmaf(w.z, relu_nan(__uint_as_float(r[h + 2])), s4[2]);
+            s4[3] = fmaf(w.w, relu_nan(__uint_as_float(r[h + 3])), s4[3]);
+          }
         }
         sc[j] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
       }
