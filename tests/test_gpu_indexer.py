@@ -129,6 +129,36 @@ def test_crowded_top_bins_with_ties(dsa, n):
     assert np.all(vals.cpu().numpy()[0] == 1024.0 * 1.625)
 
 
+def test_few_ties_at_the_threshold_take_the_lowest_positions(dsa):
+    # keys c = 1 + m/8 with c <= 1.75, exact in E4M3 under the group scale 2^-8 (codes up to
+    # 448), q = w = 1 over 8 heads, so the score is 1024 c exactly: 698 keys at c = 1.75, five
+    # at c = 1.5 (positions 50, 300, 2100, 2500, 2999) and the rest at c = 1.  With K = 700
+    # the threshold is 1536 and two of the five ties are taken: the lowest positions.  The
+    # tied keys share every bit, so the selector settles the last digit over the few
+    # candidates that share T's top bits.
+    n, K = 3000, 700
+    c = np.ones(n)
+    c[1000:1698] = 1.75
+    ties = [50, 300, 2100, 2500, 2999]
+    c[ties] = 1.5
+    k = torch.from_numpy(np.repeat(c[:, None], 128, axis=1).astype(np.float32)).to(torch.bfloat16)
+    wl = W.custom([n], h_i=8, topk=K, seed=1)
+    kc = dsa.alloc_k_cache(wl.num_pages)
+    dsa.quant_kv_mxfp8(k.cuda(), torch.from_numpy(wl.slot_mapping(0)).cuda(), kc)
+    q = torch.ones(1, 8, 128, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(1, 8, dtype=torch.float32, device="cuda")
+    vals = torch.empty(1, K, dtype=torch.float32, device="cuda")
+    idx, _ = dsa.indexer_topk(q, w, kc, torch.from_numpy(wl.page_table).cuda(),
+                              torch.tensor([n], dtype=torch.int32, device="cuda"),
+                              torch.zeros(1, dtype=torch.int32, device="cuda"),
+                              torch.tensor([n - 1], dtype=torch.int32, device="cuda"), K, n, out_scores=vals)
+    assert dsa.device_status() == 0
+    assert sorted(idx.cpu().numpy()[0].tolist()) == sorted(list(range(1000, 1698)) + ties[:2])
+    got = dict(zip(idx.cpu().numpy()[0].tolist(), vals.cpu().numpy()[0].tolist()))
+    assert all(got[p] == 1024.0 * 1.75 for p in range(1000, 1698))
+    assert got[50] == got[300] == 1024.0 * 1.5
+
+
 FULL = ["tiny", "decode_b32_ctx32k", "mixed_b128", "long_mtp_b4_ctx128k", "prefill_4k_over_64k"]
 
 
