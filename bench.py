@@ -267,13 +267,32 @@ def run_ours(args, rank, world, local_rank):
     h2d = nbytes
     d2h = out_host.numel() * out_host.element_size()
 
-    def e2e_step():
+    def e2e_eager():
         dev_buf.copy_(pin_buf, non_blocking=True)
         o, _, _ = layer.step(dd["k_new"], dd["kv_new"], dd["s_new"], dd["q_idx"], dd["w"], dd["q_sfa"],
                              dd["page_table"], dd["seq_lens"], dd["q_seq"], dd["q_pos"], wl.max_ctx,
                              wl.q_group)
         out_host.copy_(o, non_blocking=True)
         torch.cuda.current_stream().synchronize()
+
+    # the same step recorded once as a CUDA graph (copy in, decode step, copy out) through
+    # DsaDecodeLayer.capture_step, as a serving loop would replay it; the eager calls if the
+    # capture is refused
+    e2e_graph = False
+    e2e_step = e2e_eager
+    try:
+        replay = layer.capture_step(
+            dict(k_new=dd["k_new"], kv_new=dd["kv_new"], slots_new=dd["s_new"], q_idx=dd["q_idx"], w=dd["w"],
+                 q_sfa=dd["q_sfa"], page_table=dd["page_table"], seq_lens=dd["seq_lens"], q_seq=dd["q_seq"],
+                 q_pos=dd["q_pos"]),
+            wl.max_ctx, wl.q_group, stage=(pin_buf, dev_buf), result=out_host)
+
+        def e2e_step():
+            replay()
+            torch.cuda.current_stream().synchronize()
+        e2e_graph = True
+    except RuntimeError as exc:
+        print(f"e2e: graph capture refused ({exc}); timing the eager calls", file=sys.stderr)
 
     for _ in range(3):
         flush.zero_(); torch.cuda.synchronize(); e2e_step()
@@ -347,7 +366,7 @@ def run_ours(args, rank, world, local_rank):
                             "achieved_gbs": round(kv_bytes / (t_sfa * 1e-3) / 1e9, 1)},
         },
         "e2e": {"value": round(rows_per_second(n_q, world, t_e2e * 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 4)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 4), "cuda_graph": e2e_graph},
         "gpu_launches": K * launches_per_step,
         "clocks": clk,
     }

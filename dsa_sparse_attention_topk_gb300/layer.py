@@ -71,3 +71,46 @@ class DsaDecodeLayer:
                     out_idx=b["idx"], out=b["out"], out_lse=b["lse"], workspace=b["ws"],
                     stream=torch.cuda.current_stream(self.device))
         return b["out"], b["lse"], b["idx"]
+
+    def capture_step(self, inputs, max_ctx, q_group=1, stage=None, result=None):
+        """Record one decode step (``step`` on the tensors of ``inputs``) into a CUDA graph
+        and return a function that replays it on the current stream.
+
+        inputs  dict with the ``step`` arguments k_new, kv_new, slots_new, q_idx, w, q_sfa,
+                page_table, seq_lens, q_seq, q_pos: device tensors that stay in place; a
+                replay reads whatever they hold then.
+        stage   optional (pinned host tensor, device tensor) pair copied host -> device at
+                the start of every replay (the step's inputs staged in one buffer).
+        result  optional pinned host tensor [n_q, h_s, 512] bf16 that receives the output at
+                the end of every replay.
+
+        The graph holds the launches of one ``dsa_decode_step`` with their programmatic
+        dependencies, so a replay costs one graph launch instead of the host work of each
+        call.  The returned function also exposes ``out``, ``lse`` and ``idx``, the device
+        tensors the replays write.
+        """
+        keys = ("k_new", "kv_new", "slots_new", "q_idx", "w", "q_sfa", "page_table", "seq_lens", "q_seq", "q_pos")
+        args = [inputs[k] for k in keys]
+        # one eager step first: per-device queries, kernel attributes and the output buffers
+        # are set up outside the capture
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            if stage is not None:
+                stage[1].copy_(stage[0], non_blocking=True)
+            self.step(*args, max_ctx, q_group)
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        # (relaxed: the library's host-side queries during the capture are not stream work)
+        with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+            if stage is not None:
+                stage[1].copy_(stage[0], non_blocking=True)
+            out, lse, idx = self.step(*args, max_ctx, q_group)
+            if result is not None:
+                result.copy_(out, non_blocking=True)
+
+        def replay():
+            graph.replay()
+
+        replay.out, replay.lse, replay.idx, replay.graph = out, lse, idx, graph
+        return replay

@@ -177,3 +177,33 @@ def test_decode_step_equals_the_three_calls(dsa, name):
     assert torch.equal(ka, dw.k_cache) and torch.equal(va, dw.kv_cache)   # the wipe was undone
     assert torch.equal(idx_a, idx_b)
     assert torch.equal(out_a, out_b) and torch.equal(lse_a, lse_b)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode_b32_ctx32k"])
+def test_captured_step_replays_the_eager_step(dsa, name):
+    # DsaDecodeLayer.capture_step records one decode step (with a host -> device copy of
+    # staged inputs first and a device -> host copy of the output last) in a CUDA graph;
+    # its replays give the eager step's results bit for bit
+    from dsa_sparse_attention_topk_gb300.layer import DsaDecodeLayer
+    wl = W.make(name)
+    dw = DeviceWorkload(wl)
+    k_new, kv_new, s_new = _step_inputs(wl, dw)
+    layer = DsaDecodeLayer(wl.num_pages, wl.h_i, wl.h_s, wl.topk, wl.sm_scale, "cuda")
+    layer.k_cache.copy_(dw.k_cache)
+    layer.kv_cache.copy_(dw.kv_cache)
+    inputs = dict(k_new=k_new, kv_new=kv_new, slots_new=s_new, q_idx=dw.q_idx, w=dw.w, q_sfa=dw.q_sfa,
+                  page_table=dw.page_table, seq_lens=dw.seq_lens, q_seq=dw.q_seq, q_pos=dw.q_pos)
+    order = ("k_new", "kv_new", "slots_new", "q_idx", "w", "q_sfa", "page_table", "seq_lens", "q_seq", "q_pos")
+    out_e, lse_e, idx_e = [t.clone() for t in layer.step(*[inputs[k] for k in order], wl.max_ctx, wl.q_group)]
+    host_q = dw.q_sfa.cpu().pin_memory()
+    staged = torch.zeros_like(dw.q_sfa)
+    result = torch.zeros(out_e.shape, dtype=out_e.dtype).pin_memory()
+    replay = layer.capture_step(dict(inputs, q_sfa=staged), wl.max_ctx, wl.q_group, stage=(host_q, staged),
+                                result=result)
+    for _ in range(2):
+        replay()
+    torch.cuda.synchronize()
+    assert dsa.device_status() == 0
+    assert torch.equal(replay.idx, idx_e)
+    assert torch.equal(replay.out, out_e) and torch.equal(replay.lse, lse_e)
+    assert torch.equal(result, out_e.cpu())
